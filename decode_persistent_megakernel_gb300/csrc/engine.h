@@ -1,0 +1,137 @@
+// engine.h -- internal structures of the decode engine, shared by its host and device code.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+namespace tinfer {
+
+// Thread block: NCW consumer warps that compute, plus one producer warp whose elected lane streams
+// weight and K/V bytes into the shared-memory ring with bulk asynchronous copies.
+constexpr int NCW = 8;
+constexpr int NCT = NCW * 32;
+constexpr int NTHREADS = NCT + 32;
+constexpr int NR_MAX = 32;    // rows of one matrix held by one ring stage, at most
+constexpr int G_MAX = 8;      // query heads sharing one KV head, at most
+constexpr int D_MAX = 128;    // head_dim, at most
+constexpr int T_MAX = 256;    // cache slots in one attention chunk, at most
+
+enum Phase : int { PH_QKV = 0, PH_ATTN = 1, PH_O = 2, PH_GU = 3, PH_DOWN = 4, PH_LM = 5 };
+constexpr int PHASES_PER_LAYER = 5;
+
+// bits of the device error word
+enum : int {
+  EW_NONFINITE = 1,
+  EW_TIMEOUT = 2,
+  EW_BADTOKEN = 4,
+};
+
+struct LayerDev {
+  const uint8_t* qkv;   // [(nq + 2 nkv) d] packed rows of hidden inputs
+  const uint8_t* o;     // [hidden] packed rows of nq*d inputs
+  const uint8_t* gu;    // [2 ffn] packed rows (gate, up interleaved) of hidden inputs
+  const uint8_t* down;  // [hidden] packed rows of ffn inputs
+  const float* g1;      // [hidden]
+  const float* g2;      // [hidden]
+  const float* bias;    // [(nq + 2 nkv) d] or nullptr
+};
+
+struct Dims {
+  int L, H, nq, nkv, d, F, V, max_ctx;
+  int fmt;         // 0 bf16, 1 int4
+  int group;       // int4 inputs per scale
+  int scale_bf16;  // int4 scale format (0 fp16, 1 bf16)
+  float eps;
+  int rb_h, rb_qd, rb_f;  // packed row bytes for hidden, nq*d and ffn inputs
+  int rb_lm;              // bf16 LM head row bytes (2 * hidden)
+  int qkv_rows;           // (nq + 2 nkv) * d
+};
+
+// Everything one step needs; passed by value to every kernel.
+struct StepParams {
+  Dims m;
+  const LayerDev* layers;
+  const uint16_t* embed;
+  const uint16_t* lm_head;
+  const uint16_t* final_norm;
+  uint16_t* kcache;
+  uint16_t* vcache;
+  const float2* rope;      // [max_ctx][d/2] (cos, sin)
+  float* x;                // [H] residual stream
+  float* qkv;              // [qkv_rows]
+  float* attn;             // [nq * d]
+  float* act;              // [F]
+  float* part_m;           // [nq][nch_cap]
+  float* part_l;           // [nq][nch_cap]
+  float* part_o;           // [nq][nch_cap][d]
+  unsigned* tickets;       // [nkv + 1]: attention merge per KV head, then the argmax ticket
+  unsigned* gbar;          // [2]: grid barrier arrival count and generation
+  float* best_val;         // [grid]
+  int* best_idx;           // [grid]
+  int* best_bad;           // [grid]
+  int* err;                // device error word
+  int* err_host;           // mapped pinned host mirror of the error word (may be null)
+  int nch_cap;             // capacity of the partial buffers in chunks per head
+  int grid;                // CTAs
+  int ring_stages;
+  int slot_bytes;
+  long long timeout_ns;
+  // per step
+  int token;               // used when token_dev is null
+  const int* token_dev;
+  int pos;                 // used when step_dev is null
+  const int* step_dev;     // graph mode: {token, pos} written by the step's first node
+  int n_chunks_override;   // >0: fixed number of attention chunks (single-op test path)
+  float* logits;           // [V] or null
+  int* argmax;             // [1]
+  int dbg_skip_cta;        // fault injection: CTA that skips one grid-barrier arrival (-1 none)
+  int dbg_skip_barrier;
+};
+
+// Op-level GEMV description (the single-operation entry point uses the same device code).
+struct GemvOp {
+  const uint8_t* w;
+  int rows, cols, rb;
+  int fmt, group, scale_bf16;
+  const float* x;
+  const float* gain;   // nullptr: no RMSNorm prologue
+  float eps;
+  const float* bias;
+  int epi;             // TINFER_EPI_*
+  float* y;
+  int* argmax;
+};
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Packed row bytes: bf16 rows are 2*cols (cols % 8 == 0); int4 rows are cols/2 nibble bytes plus
+// 2*cols/group scale bytes, padded to 16 (cols % 32 == 0, group % 32 == 0, cols % group == 0).
+inline size_t packed_row_bytes(int fmt, int cols, int group) {
+  if (cols <= 0) return 0;
+  if (fmt == 0) return (cols % 8 == 0) ? (size_t)cols * 2 : 0;
+  if (group <= 0 || group % 32 != 0 || cols % 32 != 0 || cols % group != 0) return 0;
+  return align_up((size_t)cols / 2 + (size_t)2 * (cols / group), 16);
+}
+
+struct LayerLayout {
+  size_t off_qkv, off_o, off_gu, off_down, off_g1, off_g2, off_bias, total;
+};
+
+inline LayerLayout layer_layout(int H, int nq, int nkv, int d, int F, int fmt, int group, int bias) {
+  LayerLayout L{};
+  size_t rbh = packed_row_bytes(fmt, H, group), rbq = packed_row_bytes(fmt, nq * d, group);
+  size_t rbf = packed_row_bytes(fmt, F, group);
+  size_t qkv_rows = (size_t)(nq + 2 * nkv) * d;
+  size_t o = 0;
+  L.off_qkv = o;  o = align_up(o + qkv_rows * rbh, 256);
+  L.off_o = o;    o = align_up(o + (size_t)H * rbq, 256);
+  L.off_gu = o;   o = align_up(o + (size_t)2 * F * rbh, 256);
+  L.off_down = o; o = align_up(o + (size_t)H * rbf, 256);
+  L.off_g1 = o;   o = align_up(o + (size_t)H * 4, 256);
+  L.off_g2 = o;   o = align_up(o + (size_t)H * 4, 256);
+  L.off_bias = bias ? o : 0;
+  if (bias) o = align_up(o + qkv_rows * 4, 256);
+  L.total = o;
+  return L;
+}
+
+}  // namespace tinfer

@@ -1,0 +1,66 @@
+// kernels.h -- launch wrappers of kernels.cu, used by the host side of the engine (api.cu).
+#pragma once
+#include <cuda_runtime.h>
+
+#include "engine.h"
+
+namespace tinfer {
+
+struct OpGemvParams {
+  const uint8_t* w;
+  int rows, cols, rb;
+  int fmt, group, scale_bf16;
+  const float* x;
+  const float* gain;
+  float eps;
+  const float* bias;
+  int epi;
+  float* y;
+  int* argmax;
+  float* slot_v;
+  int* slot_i;
+  int* slot_bad;
+  unsigned* ticket;
+  int* err;
+  int stages, slot;
+  long long timeout_ns;
+};
+
+struct OpAttnParams {
+  const float* qkv;
+  uint16_t* kc;
+  uint16_t* vc;
+  const float2* rope;
+  float* part_m;
+  float* part_l;
+  float* part_o;
+  int nch_cap;
+  unsigned* tickets;
+  float* out;
+  int nq, nkv, d, max_ctx, pos, n_chunks;
+  int* err;
+  int stages, slot;
+  long long timeout_ns;
+};
+
+cudaError_t launch_megakernel(const StepParams& p, size_t smem, cudaStream_t st);
+cudaError_t launch_phase(const StepParams& p, int k, size_t smem, cudaStream_t st, bool pdl);
+cudaError_t launch_begin(int* step_dev, int token, const int* token_dev, int pos, int V, int* err,
+                         int* err_host, cudaStream_t st);
+const void* begin_kernel_fn();
+cudaError_t launch_op_gemv(const OpGemvParams& q, int grid, size_t smem, cudaStream_t st);
+cudaError_t launch_op_attention(const OpAttnParams& q, int grid, size_t smem, cudaStream_t st);
+cudaError_t set_smem_limits(size_t mega, size_t phase, size_t op);
+cudaError_t megakernel_occupancy(int* blocks_per_sm, size_t smem);
+cudaError_t phase_occupancy(int* blocks_per_sm, size_t smem);
+size_t smem_for(int stages, int slot);
+
+cudaError_t launch_pack_rows(uint8_t* dst, int dst_rb, int dst_step, int dst_first, int rows,
+                             const uint8_t* w, int w_bytes, const uint8_t* s, int s_bytes,
+                             cudaStream_t st);
+cudaError_t launch_unpack_rows(const uint8_t* src, int src_rb, int src_step, int src_first, int rows,
+                               uint8_t* w, int w_bytes, uint8_t* s, int s_bytes, cudaStream_t st);
+cudaError_t launch_bf16_to_f32(const uint16_t* in, float* out, int n, cudaStream_t st);
+cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, int n, cudaStream_t st);
+
+}  // namespace tinfer

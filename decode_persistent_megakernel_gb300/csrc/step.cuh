@@ -1,0 +1,769 @@
+// step.cuh -- device code of one decode step, shared by the persistent kernel, the per-phase
+// kernels of the CUDA-graph path and the single-operation kernels.
+//
+// Execution model. A CTA is NCW consumer warps plus one producer warp. The producer's elected lane
+// walks the CTA's static schedule (which rows of which matrix, which K/V chunks) and streams those
+// bytes from HBM into a ring of shared-memory slots with bulk asynchronous copies that complete on
+// per-slot mbarriers. Weights and cached K/V never depend on the current token ("Decoding in tiles",
+// section 1: the next kernel cannot start loading its weights although the weights never depend on
+// the token), so the producer runs ahead across phase boundaries and grid barriers, bounded only by
+// the ring; the consumers wait for the data dependency (a grid barrier) and then drain the slots.
+// This is the cross-phase weight prefetch of Hazy Research's megakernel as summarised in "Decoding
+// in tiles" (section 1 and section 4), built on Blackwell's bulk-copy engine instead of per-thread
+// loads.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <math_constants.h>
+
+#include "engine.h"
+#include "ptx.cuh"
+
+namespace tinfer {
+
+constexpr int MAX_STAGES = 8;
+
+struct Misc {
+  unsigned long long full[MAX_STAGES];
+  unsigned long long empty[MAX_STAGES];
+  float red[2][NR_MAX][NCW];   // per-stage cross-warp partial sums, double buffered
+  float wred[NCW];             // block-reduction scratch
+  float qs[G_MAX * D_MAX];     // rotated, pre-scaled queries of the current attention unit
+  float sc[G_MAX * T_MAX];     // scores, then probabilities; merge weights in the merge
+  float kn[D_MAX];             // new key of this position (bf16-rounded, as float)
+  float vn[D_MAX];             // new value of this position (bf16-rounded, as float)
+  float hm[G_MAX];
+  float hl[G_MAX];
+  float bv[NCW];
+  int bi[NCW];
+  int bbad[NCW];
+  int flag;
+  int abort;      // a consumer wait gave up: results of this step are void
+  int cons_done;  // consumers have left their loop: the producer stops issuing
+  int exit_now;   // uniform stop decision, written by consumer thread 0 between two named barriers
+};
+
+__host__ __device__ inline size_t step_smem_bytes(int stages, int slot_bytes) {
+  return (size_t)stages * slot_bytes + sizeof(Misc);
+}
+
+constexpr int BAR_CONS = 1;  // named barrier id used by the consumer warps
+
+struct Pipe {
+  uint32_t ring;    // shared address of slot 0
+  uint32_t full0;   // shared address of full[0]
+  uint32_t empty0;  // shared address of empty[0]
+  int stages;
+  int slot;
+  uint32_t it;      // stages issued (producer) or consumed (consumers)
+  Misc* ms;
+  long long timeout;
+  int* err;
+  int* err_host;
+};
+
+__device__ __forceinline__ void raise_error(int* err, int* err_host, int bits) {
+  atomicOr(err, bits);
+  if (err_host) *reinterpret_cast<volatile int*>(err_host) = bits;
+}
+
+// Waits until the phase of `parity` of mbarrier `bar` completes. Gives up after `timeout` ns, or as
+// soon as *stop is non-zero. Returns true on completion.
+__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, long long timeout,
+                                      const volatile int* stop) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*stop) return false;
+    if ((long long)(globaltimer() - t0) > timeout) return false;
+  }
+}
+
+__device__ __forceinline__ uint32_t cons_acquire(Pipe& pp) {
+  const int s = pp.it % pp.stages;
+  const uint32_t par = (pp.it / pp.stages) & 1u;
+  volatile int* ab = &pp.ms->abort;
+  if (!*ab) {
+    if (!wait_bar(pp.full0 + 8u * s, par, pp.timeout, ab)) {
+      if (!*ab) {
+        *ab = 1;
+        raise_error(pp.err, pp.err_host, EW_TIMEOUT);
+      }
+    }
+  }
+  return pp.ring + (uint32_t)s * pp.slot;
+}
+
+__device__ __forceinline__ void cons_release(Pipe& pp, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(pp.empty0 + 8u * (pp.it % pp.stages));
+  ++pp.it;
+}
+
+// Producer: one stage of `bytes` contiguous bytes (multiple of 16, <= slot) from src.
+__device__ __forceinline__ void prod_push(Pipe& pp, const void* src, uint32_t bytes, uint64_t pol,
+                                          bool& dead) {
+  if (dead) return;
+  const int s = pp.it % pp.stages;
+  const uint32_t par = ((pp.it / pp.stages) & 1u) ^ 1u;
+  if (!wait_bar(pp.empty0 + 8u * s, par, pp.timeout, &pp.ms->cons_done)) {
+    dead = true;
+    if (!*reinterpret_cast<volatile int*>(&pp.ms->cons_done))
+      raise_error(pp.err, pp.err_host, EW_TIMEOUT);
+    return;
+  }
+  const uint32_t fb = pp.full0 + 8u * s;
+  mbar_arrive_expect_tx(fb, bytes);
+  if (bytes) bulk_g2s(pp.ring + (uint32_t)s * pp.slot, src, bytes, fb, pol);
+  ++pp.it;
+}
+
+// Before the CTA exits: every copy this producer issued has landed (bounded wait).
+__device__ void prod_drain(Pipe& pp) {
+  const uint32_t n = pp.it < (uint32_t)pp.stages ? pp.it : (uint32_t)pp.stages;
+  int never = 0;
+  for (uint32_t k = pp.it - n; k < pp.it; ++k)
+    wait_bar(pp.full0 + 8u * (k % pp.stages), (k / pp.stages) & 1u, pp.timeout, &never);
+}
+
+__device__ __forceinline__ void pipe_init(Pipe& pp, unsigned char* smem, int stages, int slot,
+                                          long long timeout, int* err, int* err_host) {
+  pp.ring = smem_addr(smem);
+  pp.ms = reinterpret_cast<Misc*>(smem + (size_t)stages * slot);
+  pp.full0 = smem_addr(&pp.ms->full[0]);
+  pp.empty0 = smem_addr(&pp.ms->empty[0]);
+  pp.stages = stages;
+  pp.slot = slot;
+  pp.it = 0;
+  pp.timeout = timeout;
+  pp.err = err;
+  pp.err_host = err_host;
+}
+
+// Thread 0 initialises the barriers; call before __syncthreads.
+__device__ __forceinline__ void pipe_setup(Pipe& pp) {
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < pp.stages; ++s) {
+      mbar_init(pp.full0 + 8u * s, 1);
+      mbar_init(pp.empty0 + 8u * s, NCW);
+    }
+    pp.ms->flag = 0;
+    pp.ms->abort = 0;
+    pp.ms->cons_done = 0;
+    pp.ms->exit_now = 0;
+    mbar_fence_init();
+  }
+}
+
+// ------------------------------------------------------------------------------ small helpers
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16_to_f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+__device__ __forceinline__ uint16_t f_to_bf16_bits(float v) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+// Block-wide sum over the consumer threads; every consumer thread gets the same value (fixed
+// summation order, so the result is bit-reproducible).
+__device__ __forceinline__ float cons_block_sum(float v, Misc* ms, int tid) {
+  v = warp_sum(v);
+  if ((tid & 31) == 0) ms->wred[tid >> 5] = v;
+  named_sync(BAR_CONS, NCT);
+  float t = 0.f;
+#pragma unroll
+  for (int w = 0; w < NCW; ++w) t += ms->wred[w];
+  named_sync(BAR_CONS, NCT);
+  return t;
+}
+
+// Reduces 8 per-lane partials (8 rows) across the 32 lanes with 9 shuffles. Afterwards lanes with
+// (lane & 3) == 0 hold the warp total of row ((lane>>4)&1)*4 + ((lane>>3)&1)*2 + ((lane>>2)&1).
+__device__ __forceinline__ float transpose_reduce8(float (&v)[8], int lane) {
+  float a[4];
+  {
+    const bool up = lane & 16;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float send = up ? v[k] : v[k + 4];
+      const float keep = up ? v[k + 4] : v[k];
+      a[k] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
+    }
+  }
+  float b[2];
+  {
+    const bool up = lane & 8;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const float send = up ? a[k] : a[k + 2];
+      const float keep = up ? a[k + 2] : a[k];
+      b[k] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 8);
+    }
+  }
+  float c;
+  {
+    const bool up = lane & 4;
+    const float send = up ? b[0] : b[1];
+    const float keep = up ? b[1] : b[0];
+    c = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 4);
+  }
+  c += __shfl_xor_sync(0xFFFFFFFFu, c, 2);
+  c += __shfl_xor_sync(0xFFFFFFFFu, c, 1);
+  return c;
+}
+__device__ __forceinline__ int transpose_row8(int lane) {
+  return ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+}
+
+// ------------------------------------------------------------------------------ GEMV
+
+// 8 bf16 weights (one 16-byte chunk) dotted with 8 activations.
+__device__ __forceinline__ float dot8_bf16(const uint4 w, const float* a, float acc) {
+  acc = fmaf(bf16_lo(w.x), a[0], acc);
+  acc = fmaf(bf16_hi(w.x), a[1], acc);
+  acc = fmaf(bf16_lo(w.y), a[2], acc);
+  acc = fmaf(bf16_hi(w.y), a[3], acc);
+  acc = fmaf(bf16_lo(w.z), a[4], acc);
+  acc = fmaf(bf16_hi(w.z), a[5], acc);
+  acc = fmaf(bf16_lo(w.w), a[6], acc);
+  acc = fmaf(bf16_hi(w.w), a[7], acc);
+  return acc;
+}
+
+// 32 int4 weights (one 16-byte chunk) dotted with 32 activations, returning sum_k q_k * a_k with
+// q_k in [0, 15] (the zero point is applied by the caller). Dequantisation uses the exponent trick
+// of tinyinfer ("v0.1": OR the nibble into the mantissa of 2^23 and subtract), generalised so that
+// no shift is needed per nibble: masking nibble i of a 16-bit half in place gives the float
+// 2^23 + q * 16^i exactly, and the activation of that element is stored pre-multiplied by 16^-i
+// (exact, a power of two). (f - 2^23) * a' then equals q * a exactly before rounding, so each
+// product is rounded exactly as q * a would be. Pairs go through Blackwell's packed f32x2 units.
+__device__ __forceinline__ float dot32_int4(const uint4 w, const float* a) {
+  constexpr uint32_t MAG = 0x4B000000u;
+  const float2 B = make_float2(8388608.f, 8388608.f);
+  float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+  const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t lo = words[k], hi = words[k] >> 16;
+    const float2 f01 = make_float2(__uint_as_float((lo & 0x000Fu) | MAG), __uint_as_float((lo & 0x00F0u) | MAG));
+    const float2 f23 = make_float2(__uint_as_float((lo & 0x0F00u) | MAG), __uint_as_float((lo & 0xF000u) | MAG));
+    const float2 f45 = make_float2(__uint_as_float((hi & 0x000Fu) | MAG), __uint_as_float((hi & 0x00F0u) | MAG));
+    const float2 f67 = make_float2(__uint_as_float((hi & 0x0F00u) | MAG), __uint_as_float((hi & 0xF000u) | MAG));
+    acc0 = fma2(sub2(f01, B), make_float2(a[8 * k + 0], a[8 * k + 1]), acc0);
+    acc1 = fma2(sub2(f23, B), make_float2(a[8 * k + 2], a[8 * k + 3]), acc1);
+    acc0 = fma2(sub2(f45, B), make_float2(a[8 * k + 4], a[8 * k + 5]), acc0);
+    acc1 = fma2(sub2(f67, B), make_float2(a[8 * k + 6], a[8 * k + 7]), acc1);
+  }
+  return (acc0.x + acc0.y) + (acc1.x + acc1.y);
+}
+
+// Where the activation vector of a GEMV comes from.
+struct ActSrc {
+  const float* xf;     // fp32 source (read through L2: other CTAs wrote it in this launch)
+  const uint16_t* xb;  // or bf16 source (the embedding row)
+  const float* gf;     // fp32 RMSNorm gain, or
+  const uint16_t* gb;  // bf16 RMSNorm gain, or neither (no norm)
+  float eps;
+  int n;
+};
+
+__device__ __forceinline__ float act_x(const ActSrc& s, int i) {
+  return s.xf ? __ldcg(s.xf + i) : bf16_to_f(s.xb[i]);
+}
+__device__ __forceinline__ float act_g(const ActSrc& s, int i) {
+  return s.gf ? s.gf[i] : bf16_to_f(s.gb[i]);
+}
+
+struct GemvDesc {
+  const uint8_t* w;
+  int rows, cols, rb;
+  int fmt, group, scale_bf16;
+  int quantum;  // 2: rows come in (gate, up) pairs that one stage never splits
+};
+
+// Rows of a matrix owned by one CTA: an even split of row quanta; nr rows per ring stage.
+struct RowSplit {
+  int r0, r1, nr;
+};
+__device__ __forceinline__ RowSplit row_split(const GemvDesc& g, int cta, int grid, int slot) {
+  const int units = g.rows / g.quantum;
+  const int u0 = (int)((long long)units * cta / grid);
+  const int u1 = (int)((long long)units * (cta + 1) / grid);
+  int nr = slot / g.rb;
+  if (nr > NR_MAX) nr = NR_MAX;
+  nr -= nr % g.quantum;
+  return RowSplit{u0 * g.quantum, u1 * g.quantum, nr};
+}
+
+enum EpiKind : int { EK_STORE = 0, EK_RESIDUAL = 1, EK_SWIGLU = 2, EK_ARGMAX = 3 };
+struct Epi {
+  int kind;
+  float* y;
+  const float* bias;
+};
+
+struct Best {
+  float v;
+  int i;
+  int bad;
+};
+
+__device__ __forceinline__ void best_update(Best& b, float v, int i) {
+  if (!isfinite(v)) b.bad = 1;
+  else if (v > b.v || (v == b.v && i < b.i)) { b.v = v; b.i = i; }
+}
+
+// Consumes one CTA's rows [rs.r0, rs.r1) of a matrix from the ring. Thread layout: a row is C
+// 16-byte chunks; when C >= NCT every thread owns chunks {t, t+NCT, ...} of every row (J of them);
+// otherwise the consumer threads split into RG row groups of ceil(C/32) warps, a group owning every
+// RG-th row of a stage and a thread one chunk. Activations of a thread's chunks stay in registers
+// for the whole matrix. Per stage: each thread forms its rows' partial dot products, the warp
+// transposes-and-reduces 8 rows at a time, the warps of a group meet in shared memory, and one
+// thread per row applies the epilogue. Every reduction has a fixed order.
+template <int FMT, int J>
+__device__ void gemv_consume(Pipe& pp, const GemvDesc& g, const RowSplit& rs, const ActSrc& src,
+                             const Epi& epi, Best& best, int tid) {
+  constexpr int E = FMT == 0 ? 8 : 32;
+  Misc* ms = pp.ms;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int C = g.cols / E;
+  int RG, rg, c0, wrg;
+  if (C >= NCT) {
+    RG = 1; rg = 0; c0 = tid; wrg = NCW;
+  } else {
+    const int cpad = (C + 31) & ~31;
+    RG = NCT / cpad; rg = tid / cpad; c0 = tid % cpad; wrg = cpad / 32;
+  }
+  const bool in_group = rg < RG;
+  const int wig = warp - rg * wrg;  // warp index inside its row group
+
+  // --- activations: optional RMSNorm over the whole vector, then this thread's chunks
+  float inv = 1.f;
+  if (src.gf || src.gb) {
+    float ss = 0.f;
+    for (int i = tid; i < src.n; i += NCT) {
+      const float v = act_x(src, i);
+      ss = fmaf(v, v, ss);
+    }
+    ss = cons_block_sum(ss, ms, tid);
+    inv = 1.f / sqrtf(ss / (float)src.n + src.eps);
+  }
+  float a[J][E];
+  float S[J];
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    const int c = c0 + j * NCT;
+    const bool ok = in_group && c < C;
+    S[j] = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      float v = 0.f;
+      if (ok) {
+        v = act_x(src, c * E + e);
+        if (src.gf || src.gb) v = v * inv * act_g(src, c * E + e);
+      }
+      a[j][e] = v;
+      S[j] += v;
+    }
+    if (FMT == 1) {
+#pragma unroll
+      for (int e = 0; e < E; ++e) a[j][e] *= (e & 3) == 0 ? 1.f : (e & 3) == 1 ? 0.0625f : (e & 3) == 2 ? 0.00390625f : 0.000244140625f;
+    }
+  }
+  const uint32_t scale_off = (uint32_t)(g.cols / 2);
+
+  int buf = 0;
+  for (int s0 = rs.r0; s0 < rs.r1; s0 += rs.nr) {
+    const int nrs = min(rs.nr, rs.r1 - s0);
+    const uint32_t st = cons_acquire(pp);
+    if (in_group) {
+      const int nmine = nrs > rg ? (nrs - rg + RG - 1) / RG : 0;
+      for (int b = 0; b < nmine; b += 8) {
+        float part[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          part[q] = 0.f;
+          if (b + q < nmine) {
+            const uint32_t rowp = st + (uint32_t)(rg + RG * (b + q)) * g.rb;
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+              const int c = c0 + j * NCT;
+              if ((J == 1 || c < C) && c < C) {
+                const uint4 w = lds128(rowp + (uint32_t)c * 16u);
+                if (FMT == 0) {
+                  acc = dot8_bf16(w, a[j], acc);
+                } else {
+                  const float dq = dot32_int4(w, a[j]);
+                  const uint16_t sb = lds16(rowp + scale_off + 2u * (uint32_t)((c * 32) / g.group));
+                  const float sc = g.scale_bf16 ? bf16_to_f(sb) : __half2float(__ushort_as_half(sb));
+                  acc = fmaf(sc, dq - 8.f * S[j], acc);
+                }
+              }
+            }
+            part[q] = acc;
+          }
+        }
+        const float v = transpose_reduce8(part, lane);
+        const int q8 = transpose_row8(lane);
+        if ((lane & 3) == 0 && b + q8 < nmine) ms->red[buf][rg + RG * (b + q8)][wig] = v;
+      }
+    }
+    cons_release(pp, lane);
+    named_sync(BAR_CONS, NCT);
+    if (epi.kind == EK_SWIGLU) {
+      if (tid < nrs / 2) {
+        float gt = 0.f, up = 0.f;
+        for (int w = 0; w < wrg; ++w) gt += ms->red[buf][2 * tid][w];
+        for (int w = 0; w < wrg; ++w) up += ms->red[buf][2 * tid + 1][w];
+        epi.y[s0 / 2 + tid] = gt / (1.f + expf(-gt)) * up;
+      }
+    } else if (tid < nrs) {
+      float v = 0.f;
+      for (int w = 0; w < wrg; ++w) v += ms->red[buf][tid][w];
+      const int r = s0 + tid;
+      if (epi.kind == EK_STORE) {
+        epi.y[r] = epi.bias ? v + epi.bias[r] : v;
+      } else if (epi.kind == EK_RESIDUAL) {
+        epi.y[r] += v;
+      } else {  // EK_ARGMAX
+        if (epi.y) epi.y[r] = v;
+        best_update(best, v, r);
+      }
+    }
+    buf ^= 1;
+  }
+}
+
+// Runtime dispatch to the template instance for (format, chunks per thread).
+__device__ __noinline__ void gemv_consume_any(Pipe& pp, const GemvDesc& g, const RowSplit& rs,
+                                              const ActSrc& src, const Epi& epi, Best& best,
+                                              int tid) {
+  if (g.fmt == 1) {
+    gemv_consume<1, 1>(pp, g, rs, src, epi, best, tid);
+    return;
+  }
+  const int C = g.cols / 8;
+  const int J = (C + NCT - 1) / NCT;
+  switch (J) {
+    case 1: gemv_consume<0, 1>(pp, g, rs, src, epi, best, tid); break;
+    case 2: gemv_consume<0, 2>(pp, g, rs, src, epi, best, tid); break;
+    case 3: gemv_consume<0, 3>(pp, g, rs, src, epi, best, tid); break;
+    case 4: gemv_consume<0, 4>(pp, g, rs, src, epi, best, tid); break;
+    default: gemv_consume<0, 5>(pp, g, rs, src, epi, best, tid); break;
+  }
+}
+
+__device__ __forceinline__ void produce_rows(Pipe& pp, const GemvDesc& g, const RowSplit& rs,
+                                             uint64_t pol, bool& dead) {
+  for (int s0 = rs.r0; s0 < rs.r1; s0 += rs.nr) {
+    const int nrs = min(rs.nr, rs.r1 - s0);
+    prod_push(pp, g.w + (size_t)s0 * g.rb, (uint32_t)(nrs * g.rb), pol, dead);
+  }
+}
+
+// Per-CTA (max, lowest index, non-finite) over the consumer threads. Result valid in thread 0.
+__device__ __forceinline__ Best best_block_reduce(Best b, Misc* ms, int tid) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xFFFFFFFFu, b.v, o);
+    const int oi = __shfl_xor_sync(0xFFFFFFFFu, b.i, o);
+    const int ob = __shfl_xor_sync(0xFFFFFFFFu, b.bad, o);
+    if (ov > b.v || (ov == b.v && oi < b.i)) { b.v = ov; b.i = oi; }
+    b.bad |= ob;
+  }
+  if ((tid & 31) == 0) { ms->bv[tid >> 5] = b.v; ms->bi[tid >> 5] = b.i; ms->bbad[tid >> 5] = b.bad; }
+  named_sync(BAR_CONS, NCT);
+  Best r{-CUDART_INF_F, 0x7FFFFFFF, 0};
+  if (tid == 0) {
+    for (int w = 0; w < NCW; ++w) {
+      if (ms->bv[w] > r.v || (ms->bv[w] == r.v && ms->bi[w] < r.i)) { r.v = ms->bv[w]; r.i = ms->bi[w]; }
+      r.bad |= ms->bbad[w];
+    }
+  }
+  named_sync(BAR_CONS, NCT);
+  return r;
+}
+
+// Argmax across CTAs: each CTA publishes its best in slot `cta`; the last CTA to take a ticket
+// combines all slots (order-independent: max value, then lowest index) and writes the token, or -1
+// and the non-finite error bit ("Decoding in tiles", section 5: per-task best candidates, lowest
+// token id among ties, an error word on a non-finite logit).
+__device__ void argmax_publish(const Best& mine, float* slot_v, int* slot_i, int* slot_bad,
+                               unsigned* ticket, int nslots, int cta, int* out, int* err,
+                               int* err_host, Misc* ms, int tid) {
+  if (tid == 0) {
+    slot_v[cta] = mine.v;
+    slot_i[cta] = mine.i;
+    slot_bad[cta] = mine.bad;
+    __threadfence();
+    const unsigned old = atomicAdd(ticket, 1u);
+    ms->flag = (old == (unsigned)nslots - 1);
+  }
+  named_sync(BAR_CONS, NCT);
+  if (ms->flag && tid < 32) {
+    __threadfence();
+    Best b{-CUDART_INF_F, 0x7FFFFFFF, 0};
+    for (int s = tid; s < nslots; s += 32) {
+      const float v = __ldcg(slot_v + s);
+      const int i = __ldcg(slot_i + s);
+      if (v > b.v || (v == b.v && i < b.i)) { b.v = v; b.i = i; }
+      b.bad |= __ldcg(slot_bad + s);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xFFFFFFFFu, b.v, o);
+      const int oi = __shfl_xor_sync(0xFFFFFFFFu, b.i, o);
+      const int ob = __shfl_xor_sync(0xFFFFFFFFu, b.bad, o);
+      if (ov > b.v || (ov == b.v && oi < b.i)) { b.v = ov; b.i = oi; }
+      b.bad |= ob;
+    }
+    if (tid == 0) {
+      *out = b.bad ? -1 : b.i;
+      if (b.bad) raise_error(err, err_host, EW_NONFINITE);
+      atomicExch(ticket, 0u);
+    }
+  }
+  named_sync(BAR_CONS, NCT);
+}
+
+// ------------------------------------------------------------------------------ attention
+
+struct AttnSplit {
+  int nch;  // chunks per KV head
+  int cl;   // slots per chunk
+};
+
+// Split of [0, pos] into chunks: enough chunks that KV heads x chunks covers the grid, each chunk
+// no longer than one ring slot holds (and T_MAX); trailing chunks may be empty.
+__device__ __forceinline__ AttnSplit attn_split(int pos, int nkv, int d, int grid, int slot,
+                                                int override_nch) {
+  const int n_ctx = pos + 1;
+  int tmax = slot / (2 * d);
+  if (tmax > T_MAX) tmax = T_MAX;
+  int nch;
+  if (override_nch > 0) {
+    nch = override_nch;
+  } else {
+    const int nmin = (n_ctx + tmax - 1) / tmax;
+    int want = grid / nkv;
+    if (want < 1) want = 1;
+    if (want > n_ctx) want = n_ctx;
+    if (want > T_MAX) want = T_MAX;
+    nch = nmin > want ? nmin : want;
+  }
+  return AttnSplit{nch, (n_ctx + nch - 1) / nch};
+}
+
+struct AttnArgs {
+  const float* qkv;        // [q | k | v] raw projections
+  uint16_t* kc;            // this layer's K cache [nkv][max_ctx][d]
+  uint16_t* vc;
+  const float2* rope;      // [max_ctx][d/2]
+  float* part_m;
+  float* part_l;
+  float* part_o;
+  int nch_cap;
+  unsigned* tickets;       // [nkv]
+  float* out;              // [nq * d]
+  int nq, nkv, d, max_ctx, pos;
+};
+
+__device__ __forceinline__ void produce_attn_unit(Pipe& pp, const AttnArgs& A, int j, int c,
+                                                  const AttnSplit& sp, uint64_t pol, bool& dead) {
+  const int t0 = c * sp.cl;
+  int tend = t0 + sp.cl;
+  if (tend > A.pos) tend = A.pos;  // the slot at pos is written in this step: never streamed
+  const int nk = tend > t0 ? tend - t0 : 0;
+  const size_t base = ((size_t)j * A.max_ctx + t0) * A.d;
+  prod_push(pp, A.kc + base, (uint32_t)(nk * A.d * 2), pol, dead);
+  prod_push(pp, A.vc + base, (uint32_t)(nk * A.d * 2), pol, dead);
+}
+
+// Merge of one KV head's chunk partials for its query heads (the log-sum-exp combine).
+__device__ void attn_merge(const AttnArgs& A, Misc* ms, int tid, int j, int nch) {
+  const int G = A.nq / A.nkv, d = A.d;
+  const int warp = tid >> 5, lane = tid & 31;
+  if (warp < G) {
+    const int h = j * G + warp;
+    float M = -CUDART_INF_F;
+    for (int c = lane; c < nch; c += 32) M = fmaxf(M, __ldcg(A.part_m + (size_t)h * A.nch_cap + c));
+    M = warp_max(M);
+    float den = 0.f;
+    for (int c = lane; c < nch; c += 32) {
+      const float mc = __ldcg(A.part_m + (size_t)h * A.nch_cap + c);
+      float w = 0.f;
+      if (mc != -CUDART_INF_F) w = expf(mc - M);  // an empty chunk weighs exactly 0
+      ms->sc[warp * T_MAX + c] = w;
+      den = fmaf(w, __ldcg(A.part_l + (size_t)h * A.nch_cap + c), den);
+    }
+    den = warp_sum(den);
+    if (lane == 0) ms->hl[warp] = 1.f / den;
+  }
+  named_sync(BAR_CONS, NCT);
+  for (int idx = tid; idx < G * d; idx += NCT) {
+    const int g = idx / d, i = idx - g * d;
+    const int h = j * G + g;
+    const float* po = A.part_o + (size_t)h * A.nch_cap * d + i;
+    float acc = 0.f;
+    for (int c = 0; c < nch; ++c) acc = fmaf(ms->sc[g * T_MAX + c], __ldcg(po + (size_t)c * d), acc);
+    A.out[(size_t)h * d + i] = acc * ms->hl[g];
+  }
+}
+
+// One attention unit: KV head j, chunk c. RoPE on the group's queries (and, in the chunk holding
+// pos, on the new key, which is written to the cache with the new value), scores over the chunk,
+// per-head max / exponentials / sum, the value sum, and the partial (m, l, o) of the chunk
+// ("One launch per token", "The attention trap"; tinyinfer, "Round 2": one block per KV head and
+// chunk serving all grouped query heads, K/V read once). The last CTA done with head j merges.
+__device__ void attn_unit(Pipe& pp, const AttnArgs& A, const AttnSplit& sp, int j, int c, int tid) {
+  Misc* ms = pp.ms;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int d = A.d, half = d / 2, G = A.nq / A.nkv;
+  const int pos = A.pos, n_ctx = pos + 1;
+  const int t0 = c * sp.cl;
+  const int t1 = min(t0 + sp.cl, n_ctx);
+  const bool has_pos = t0 <= pos && pos < t1;
+  const int nk = max(0, min(t1, pos) - t0);
+  const int T = max(0, t1 - t0);
+  const float scale = 1.f / sqrtf((float)d);
+  const float2* rt = A.rope + (size_t)pos * half;
+  const float* q = A.qkv + (size_t)j * G * d;
+  const float* kr = A.qkv + (size_t)A.nq * d + (size_t)j * d;
+  const float* vr = kr + (size_t)A.nkv * d;
+
+  for (int idx = tid; idx < G * half; idx += NCT) {
+    const int g = idx / half, i = idx - g * half;
+    const float x0 = __ldcg(q + g * d + i), x1 = __ldcg(q + g * d + i + half);
+    const float2 cs = rt[i];
+    ms->qs[g * d + i] = (x0 * cs.x - x1 * cs.y) * scale;
+    ms->qs[g * d + i + half] = (x1 * cs.x + x0 * cs.y) * scale;
+  }
+  if (has_pos) {
+    const size_t slot = ((size_t)j * A.max_ctx + pos) * d;
+    for (int i = tid; i < half; i += NCT) {
+      const float x0 = __ldcg(kr + i), x1 = __ldcg(kr + i + half);
+      const float2 cs = rt[i];
+      const uint16_t b0 = f_to_bf16_bits(x0 * cs.x - x1 * cs.y);
+      const uint16_t b1 = f_to_bf16_bits(x1 * cs.x + x0 * cs.y);
+      A.kc[slot + i] = b0;
+      A.kc[slot + i + half] = b1;
+      ms->kn[i] = bf16_to_f(b0);
+      ms->kn[i + half] = bf16_to_f(b1);
+    }
+    for (int i = tid; i < d; i += NCT) {
+      const uint16_t b = f_to_bf16_bits(__ldcg(vr + i));
+      A.vc[slot + i] = b;
+      ms->vn[i] = bf16_to_f(b);
+    }
+  }
+  named_sync(BAR_CONS, NCT);
+
+  // scores: one thread per cached slot; 16-byte chunks of the key row visited in a rotated order
+  // so that the 8 lanes of a quarter-warp hit distinct banks
+  const uint32_t kst = cons_acquire(pp);
+  const int nc = d / 8;
+  if (tid < nk) {
+    float s[G_MAX];
+#pragma unroll
+    for (int g = 0; g < G_MAX; ++g) s[g] = 0.f;
+    const uint32_t row = kst + (uint32_t)tid * d * 2;
+    for (int cc = 0; cc < nc; ++cc) {
+      const int ch = (cc + tid) % nc;
+      const uint4 kv = lds128(row + ch * 16);
+      const float k8[8] = {bf16_lo(kv.x), bf16_hi(kv.x), bf16_lo(kv.y), bf16_hi(kv.y),
+                           bf16_lo(kv.z), bf16_hi(kv.z), bf16_lo(kv.w), bf16_hi(kv.w)};
+#pragma unroll
+      for (int g = 0; g < G_MAX; ++g) {
+        if (g < G) {
+          const float* qg = ms->qs + g * d + ch * 8;
+          float t = s[g];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) t = fmaf(qg[e], k8[e], t);
+          s[g] = t;
+        }
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < G_MAX; ++g)
+      if (g < G) ms->sc[g * T_MAX + tid] = s[g];
+  }
+  if (has_pos && tid == nk) {
+    for (int g = 0; g < G; ++g) {
+      float t = 0.f;
+      for (int i = 0; i < d; ++i) t = fmaf(ms->qs[g * d + i], ms->kn[i], t);
+      ms->sc[g * T_MAX + nk] = t;
+    }
+  }
+  cons_release(pp, lane);
+  named_sync(BAR_CONS, NCT);
+
+  if (warp < G) {
+    float m = -CUDART_INF_F;
+    for (int t = lane; t < T; t += 32) m = fmaxf(m, ms->sc[warp * T_MAX + t]);
+    m = warp_max(m);
+    float l = 0.f;
+    for (int t = lane; t < T; t += 32) {
+      const float e = expf(ms->sc[warp * T_MAX + t] - m);
+      ms->sc[warp * T_MAX + t] = e;
+      l += e;
+    }
+    l = warp_sum(l);
+    if (lane == 0) { ms->hm[warp] = m; ms->hl[warp] = l; }
+  }
+  named_sync(BAR_CONS, NCT);
+
+  const uint32_t vst = cons_acquire(pp);
+  for (int idx = tid; idx < G * half; idx += NCT) {
+    const int g = idx / half, i2 = idx - g * half;
+    const float* pg = ms->sc + g * T_MAX;
+    float o0 = 0.f, o1 = 0.f;
+    for (int t = 0; t < nk; ++t) {
+      const uint32_t vv = lds32(vst + (uint32_t)(t * d + 2 * i2) * 2u);
+      o0 = fmaf(pg[t], bf16_lo(vv), o0);
+      o1 = fmaf(pg[t], bf16_hi(vv), o1);
+    }
+    if (has_pos) {
+      o0 = fmaf(pg[nk], ms->vn[2 * i2], o0);
+      o1 = fmaf(pg[nk], ms->vn[2 * i2 + 1], o1);
+    }
+    const int h = j * G + g;
+    float2* po = reinterpret_cast<float2*>(A.part_o + ((size_t)h * A.nch_cap + c) * d) + i2;
+    *po = make_float2(o0, o1);
+  }
+  cons_release(pp, lane);
+  if (tid < G) {
+    const int h = j * G + tid;
+    A.part_m[(size_t)h * A.nch_cap + c] = ms->hm[tid];
+    A.part_l[(size_t)h * A.nch_cap + c] = ms->hl[tid];
+  }
+  __threadfence();
+  named_sync(BAR_CONS, NCT);
+  if (tid == 0) {
+    const unsigned old = atomicAdd(A.tickets + j, 1u);
+    ms->flag = (old == (unsigned)sp.nch - 1);
+  }
+  named_sync(BAR_CONS, NCT);
+  if (ms->flag) {
+    __threadfence();
+    attn_merge(A, ms, tid, j, sp.nch);
+    if (tid == 0) atomicExch(A.tickets + j, 0u);
+  }
+  named_sync(BAR_CONS, NCT);
+}
+
+}  // namespace tinfer

@@ -1,0 +1,197 @@
+/* tinfer.h -- C ABI of the GB300 batch-1 decode engine.
+ *
+ * One call runs one decode step of a Llama-family dense transformer for a single sequence:
+ * embedding, every decoder layer (RMSNorm, fused QKV GEMV, NEOX RoPE plus K/V append, grouped-query
+ * split-K attention with a log-sum-exp merge, O GEMV plus residual, RMSNorm, gate/up GEMV with
+ * SwiGLU, down GEMV plus residual), final RMSNorm, LM head and greedy argmax. The problem statement
+ * follows "Decoding in tiles" (TileInfer), sections 4-5 (create once, launch per token, greedy
+ * choice on the device) and "One launch per token", section "Slow, because the launches are still
+ * there" (token and position handed to a fixed-shape step).
+ *
+ * Conventions for every entry point:
+ *   - Pointers named *_dev are device pointers (cudaMalloc or equivalent); *_host are host
+ *     pointers. `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *   - Every call returns a tinfer_status and never aborts the process. Host-side validation
+ *     failures return TINFER_ERR_INVALID_ARG / TINFER_ERR_UNSUPPORTED before anything is launched.
+ *   - Work is asynchronous on `stream` unless stated otherwise. Device-side failures (a non-finite
+ *     logit, a synchronisation wait that ran out) are recorded in the context's error word; the
+ *     next tinfer_decode_step* call returns them without launching, and tinfer_get_error reports
+ *     and clears them.
+ *   - Matrices are row-major [rows = outputs][cols = inputs]. bf16 values are IEEE bfloat16 bit
+ *     patterns. int4 matrices are [rows][cols/2] bytes, input element 2j in the low nibble of byte
+ *     j and 2j+1 in the high nibble, value (q - 8) * scale, one fp16 or bf16 scale per `group_size`
+ *     consecutive inputs of a row ([rows][cols/group] scales). This is the canonical layout; the
+ *     engine streams its own packed layout, made by tinfer_pack_layer.
+ *   - The KV cache is two caller-owned bf16 buffers, K and V, each [n_layers][n_kv_heads][max_ctx]
+ *     [head_dim]. Position `pos` is 0-based; a step at `pos` writes slot `pos` of every layer and
+ *     attends over slots [0, pos], so slots [0, pos) must hold earlier keys/values.
+ */
+#ifndef TINFER_H
+#define TINFER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TINFER_OK = 0,
+  TINFER_ERR_INVALID_ARG = 1,   /* a pointer, size, token or position outside its contract */
+  TINFER_ERR_UNSUPPORTED = 2,   /* a shape or format this build does not handle */
+  TINFER_ERR_CUDA = 3,          /* a CUDA runtime call failed (launch, capture, copy) */
+  TINFER_ERR_OOM = 4,           /* a device or pinned-host allocation failed */
+  TINFER_ERR_NONFINITE = 5,     /* a logit was NaN or infinite (the argmax output is -1) */
+  TINFER_ERR_TIMEOUT = 6        /* a device-side wait gave up (grid barrier, pipeline stage) */
+} tinfer_status;
+
+enum { TINFER_BF16 = 0, TINFER_INT4 = 1 };              /* weight_format */
+enum { TINFER_SCALE_FP16 = 0, TINFER_SCALE_BF16 = 1 };  /* scale_dtype (int4 only) */
+enum { TINFER_MEGAKERNEL = 0, TINFER_GRAPH = 1 };       /* exec_mode */
+
+typedef struct {
+  int n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn, vocab, max_ctx;
+  double rope_theta;   /* RoPE base; angle of pair i at position p is p * theta^(-2i/head_dim) */
+  double rms_eps;      /* RMSNorm epsilon inside the square root */
+  int weight_format;   /* TINFER_BF16 or TINFER_INT4 (int4 covers q,k,v,o,gate,up,down) */
+  int group_size;      /* int4: inputs per scale; a multiple of 32 dividing hidden, n_heads*head_dim, ffn */
+  int scale_dtype;     /* int4: TINFER_SCALE_FP16 or TINFER_SCALE_BF16 */
+  int tied_embeddings; /* informational: lm_head may equal embed */
+  int qkv_bias;        /* 1: bf16 biases are added to q, k, v before RoPE */
+  int exec_mode;       /* TINFER_MEGAKERNEL (one persistent launch per step) or TINFER_GRAPH */
+} tinfer_config;
+
+/* Canonical per-layer weights (device pointers), the input of tinfer_pack_layer.
+ * w*: bf16 [rows][cols] or int4 bytes [rows][cols/2]; s*: int4 scales (NULL for bf16);
+ * b*: bf16 biases of length rows (NULL unless qkv_bias); g1, g2: bf16 RMSNorm gains [hidden]. */
+typedef struct {
+  const void *wq, *wk, *wv, *wo, *wg, *wu, *wd;
+  const void *sq, *sk, *sv, *so, *sg, *su, *sd;
+  const void *bq, *bk, *bv;
+  const void *g1, *g2;
+} tinfer_layer_src;
+
+/* Model weights for tinfer_create (device pointers, borrowed: they must outlive the context).
+ * embed, lm_head: bf16 [vocab][hidden] (lm_head may equal embed); final_norm: bf16 [hidden];
+ * layer_blobs: HOST array of n_layers device pointers, each a packed layer made by
+ * tinfer_pack_layer (16-byte aligned, tinfer_packed_layer_bytes long). */
+typedef struct {
+  const void* embed;
+  const void* lm_head;
+  const void* final_norm;
+  const void* const* layer_blobs;
+} tinfer_weights;
+
+typedef struct tinfer_ctx tinfer_ctx;
+
+const char* tinfer_status_string(tinfer_status s);
+
+/* Validates a configuration without allocating anything. */
+tinfer_status tinfer_check_config(const tinfer_config* cfg);
+
+/* Offline weight packer (the "concatenate QKV and gate/up at load" step of tinyinfer, "Round 3:
+ * fusion", and "One launch per token", "The oracle, then the kernels"). The packed layer holds, in
+ * order and 256-byte aligned: [Wq;Wk;Wv] rows, Wo rows, gate/up rows interleaved (row 2i = gate i,
+ * row 2i+1 = up i), Wd rows, g1 and g2 as fp32, and the QKV bias as fp32. Every row is padded to a
+ * multiple of 16 bytes; an int4 row stores its cols/2 nibble bytes followed by its cols/group scales.
+ * tinfer_packed_layer_bytes returns 0 for an invalid config. pack writes packed_dev (caller-owned,
+ * 16-byte aligned) on `stream`; unpack inverts it into the canonical buffers of dst (the bytes of
+ * every weight, scale, bias and gain reproduced exactly; gains and biases round-trip through fp32
+ * exactly). */
+size_t tinfer_packed_layer_bytes(const tinfer_config* cfg);
+tinfer_status tinfer_pack_layer(const tinfer_config* cfg, const tinfer_layer_src* src,
+                                void* packed_dev, void* stream);
+tinfer_status tinfer_unpack_layer(const tinfer_config* cfg, const void* packed_dev,
+                                  const tinfer_layer_src* dst, void* stream);
+
+/* Creates an engine over borrowed weights and a borrowed KV cache (k_cache_dev, v_cache_dev: bf16
+ * [n_layers][n_kv_heads][max_ctx][head_dim]). The context owns its scratch (activations, split-K
+ * partials, barrier and ticket words, argmax slots, the fp32 RoPE cos/sin table, the CUDA graph in
+ * graph mode) and frees it in tinfer_destroy. Uses the current CUDA device. */
+tinfer_status tinfer_create(const tinfer_config* cfg, const tinfer_weights* w, void* k_cache_dev,
+                            void* v_cache_dev, tinfer_ctx** out);
+
+/* One decode step for token_id at position pos on `stream`. logits_dev (fp32 [vocab]) may be NULL
+ * to skip writing the logits; argmax_dev (int32 [1]) receives the greedy token, the lowest id among
+ * equal maxima, or -1 when a logit is non-finite. Returns at once (asynchronous). */
+tinfer_status tinfer_decode_step(tinfer_ctx* ctx, int32_t token_id, int32_t pos, void* stream,
+                                 float* logits_dev, int32_t* argmax_dev);
+
+/* Same step, but the token id is read on the device from token_dev (int32 [1]) when the step runs,
+ * so that greedy decoding can chain steps without a host round trip (token_dev may be the previous
+ * step's argmax_dev). An out-of-range device token sets TINFER_ERR_INVALID_ARG in the error word. */
+tinfer_status tinfer_decode_step_dev(tinfer_ctx* ctx, const int32_t* token_dev, int32_t pos,
+                                     void* stream, float* logits_dev, int32_t* argmax_dev);
+
+/* Greedy generation with the host in the loop: for k in [0, n_steps) the step at pos0 + k is fed
+ * (from pinned host memory) token first_token for k = 0 and the previous step's choice after that;
+ * each step's choice is copied back to the host and written to tokens_host[k]. Synchronous: returns
+ * when all steps are done. */
+tinfer_status tinfer_generate(tinfer_ctx* ctx, int32_t first_token, int32_t pos0, int32_t n_steps,
+                              void* stream, int32_t* tokens_host);
+
+/* Waits for all work of the context, then returns and clears the device error word
+ * (TINFER_OK if none). Clearing also resets the context's barrier and ticket words. */
+tinfer_status tinfer_get_error(tinfer_ctx* ctx);
+
+/* Introspection: TINFER_Q_GRID (CTAs of the persistent launch = SM count), TINFER_Q_SMEM (dynamic
+ * shared memory per CTA of the persistent kernel), TINFER_Q_RING_STAGES, TINFER_Q_SLOT_BYTES,
+ * TINFER_Q_KERNELS_PER_STEP (kernel launches one step makes). Returns -1 for an unknown query. */
+enum { TINFER_Q_GRID = 0, TINFER_Q_SMEM = 1, TINFER_Q_RING_STAGES = 2, TINFER_Q_SLOT_BYTES = 3,
+       TINFER_Q_KERNELS_PER_STEP = 4 };
+long long tinfer_query(const tinfer_ctx* ctx, int what);
+
+/* Test hooks: timeout of every device-side wait in nanoseconds (default 200 ms), and a fault
+ * injected on the host side of the contract: CTA `cta` skips its arrival at grid barrier number
+ * `barrier` of the next persistent step, so that the other CTAs' waits run out and the step
+ * reports TINFER_ERR_TIMEOUT (cta = -1 disables). */
+tinfer_status tinfer_set_timeout_ns(tinfer_ctx* ctx, long long ns);
+tinfer_status tinfer_debug_skip_barrier(tinfer_ctx* ctx, int cta, int barrier);
+
+void tinfer_destroy(tinfer_ctx* ctx);
+
+/* ---------------------------------------------------------------------------------------------
+ * Single-operation entry points. They run the same device code as the step, one operation at a
+ * time, for the per-kernel parity tests. All pointers are device pointers owned by the caller.
+ * --------------------------------------------------------------------------------------------- */
+
+/* Bytes of one packed row of `cols` inputs (0 if the format cannot hold that width). */
+size_t tinfer_packed_row_bytes(int weight_format, int cols, int group_size);
+
+/* Packs a canonical matrix (bf16, or int4 bytes plus scales) into packed rows. */
+tinfer_status tinfer_pack_matrix(int weight_format, int group_size, int scale_dtype, int rows,
+                                 int cols, const void* w_dev, const void* scales_dev,
+                                 void* packed_dev, void* stream);
+
+enum { TINFER_EPI_STORE = 0, TINFER_EPI_RESIDUAL = 1, TINFER_EPI_SWIGLU = 2, TINFER_EPI_ARGMAX = 3 };
+
+/* y = W a through the streaming GEMV (TMA bulk copies into a shared-memory ring, fp32 accumulate).
+ * a = x, or a = rmsnorm(x) * gain when gain_dev (fp32 [cols]) is not NULL (eps = rms_eps).
+ * Epilogue: STORE y[r] = v (+ bias_dev[r] if not NULL); RESIDUAL y[r] += v; SWIGLU: rows come in
+ * (gate, up) pairs, y[i] = silu(v[2i]) * v[2i+1] (rows must be even); ARGMAX: y[r] = v (y may be
+ * NULL) and argmax_dev[0] = the lowest row among the maxima, or -1 and TINFER_ERR_NONFINITE if any v
+ * is non-finite. x_dev: fp32 [cols]. Synchronises `stream` for ARGMAX so that the status is exact. */
+tinfer_status tinfer_op_gemv(int weight_format, int group_size, int scale_dtype, int rows, int cols,
+                             const void* packed_dev, const float* x_dev, const float* gain_dev,
+                             double rms_eps, const float* bias_dev, int epilogue, float* y_dev,
+                             int32_t* argmax_dev, void* stream);
+
+/* Attention for one layer at position pos: qkv_dev holds the raw projections [q (n_heads*head_dim) |
+ * k (n_kv_heads*head_dim) | v (n_kv_heads*head_dim)] in fp32 (bias already added). The op applies
+ * RoPE (fp32 cos/sin table built on the host in double from rope_theta) to q and k, writes
+ * bf16(k_rot) and bf16(v) to slot pos of k_layer_dev / v_layer_dev ([n_kv_heads][max_ctx][head_dim]),
+ * runs split-K attention over [0, pos] in n_chunks chunks of ceil((pos+1)/n_chunks) slots (n_chunks
+ * = 0: the engine's own choice) and merges the partials into out_dev (fp32 [n_heads*head_dim]).
+ * part_m_dev, part_l_dev ([n_heads][n_chunks]) and part_o_dev ([n_heads][n_chunks][head_dim]) may be
+ * NULL; when given (with explicit n_chunks) they receive the unnormalised partials. */
+tinfer_status tinfer_op_attention(int n_heads, int n_kv_heads, int head_dim, int max_ctx,
+                                  double rope_theta, int pos, int n_chunks, const float* qkv_dev,
+                                  void* k_layer_dev, void* v_layer_dev, float* out_dev,
+                                  float* part_m_dev, float* part_l_dev, float* part_o_dev,
+                                  void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TINFER_H */

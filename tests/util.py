@@ -1,0 +1,40 @@
+"""Shared helpers of the tests: bf16 views, tolerances and the teacher-forced step comparison."""
+import numpy as np
+
+# Tolerances on logits between the CUDA path (fp32 accumulation) and the fp64 oracle, as the
+# benchmark's acceptance bar states them.
+LOGIT_MAX_ABS = 2e-2
+LOGIT_REL_L2 = 5e-3
+ARGMAX_MARGIN = 5e-2
+
+
+def bf16_to_f64(bits):
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def f32_to_bf16_bits(x):
+    """Round-to-nearest-even float32 -> bf16 bits (numpy, for building test inputs)."""
+    x = np.asarray(x, np.float32)
+    u = x.view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+    return r
+
+
+def compare_logits(got, ref):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    err = float(np.abs(got - ref).max())
+    rel = float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
+    srt = np.sort(ref)
+    margin = float(srt[-1] - srt[-2])
+    return err, rel, margin
+
+
+def ulp_diff_bf16(a, b):
+    """Distance in bf16 steps between two arrays of bf16 bit patterns (same sign assumed)."""
+    a = np.asarray(a, np.uint16).astype(np.int32)
+    b = np.asarray(b, np.uint16).astype(np.int32)
+    # map sign-magnitude to a monotone integer line
+    ma = np.where(a & 0x8000, -(a & 0x7FFF), a & 0x7FFF)
+    mb = np.where(b & 0x8000, -(b & 0x7FFF), b & 0x7FFF)
+    return np.abs(ma - mb)
