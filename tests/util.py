@@ -38,3 +38,17 @@ def ulp_diff_bf16(a, b):
     ma = np.where(a & 0x8000, -(a & 0x7FFF), a & 0x7FFF)
     mb = np.where(b & 0x8000, -(b & 0x7FFF), b & 0x7FFF)
     return np.abs(ma - mb)
+
+
+def kv_close(gpu_bits, ref_bits, rel_floor=2e-4):
+    """KV values written by the GPU (fp32 arithmetic, rounded to bf16) against the oracle's (fp64,
+    rounded to bf16): equal up to one bf16 step at that magnitude, plus an absolute floor of
+    rel_floor x the RMS of the reference values. The floor covers values near zero, where the fp32
+    error carried by the residual stream and a long dot product exceeds a bf16 step; a wrong
+    rotation, sign or slot errs by O(RMS) and still fails. Returns the worst excess (<= 0 when every
+    value is close)."""
+    a = bf16_to_f64(gpu_bits)
+    b = bf16_to_f64(ref_bits)
+    floor = rel_floor * float(np.sqrt(np.mean(b * b)))
+    tol = np.maximum(np.abs(a), np.abs(b)) * 2.0 ** -7 + floor
+    return float((np.abs(a - b) - tol).max())
