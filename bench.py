@@ -206,6 +206,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-read-probe", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=0, help="steps of the e2e run (default: the workload's)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -256,14 +258,15 @@ def main():
         if name == modes[0][0]:
             # end to end through the public call: host-in-the-loop greedy generation, one pinned
             # 4-byte token copied in and one 4-byte choice copied out per step
-            out = np.zeros(S, dtype=np.int32)
+            n_e2e = min(S, args.e2e_steps) if args.e2e_steps > 0 else S
+            out = np.zeros(n_e2e, dtype=np.int32)
             barrier(dist, torch)
             t0 = time.perf_counter()
-            rc = T.tinfer_generate(eng.ctx, first, P, S, st, out)
+            rc = T.tinfer_generate(eng.ctx, first, P, n_e2e, st, out)
             el = time.perf_counter() - t0
             assert rc == 0
             el = max_over_ranks(dist, torch, el)
-            results["e2e"] = dict(value=world * S / el, steps=S)
+            results["e2e"] = dict(value=world * n_e2e / el, steps=n_e2e)
         eng.close()
         del eng
         torch.cuda.empty_cache()
@@ -271,6 +274,8 @@ def main():
     # a pure streaming-read probe (page 1's yardstick), same process
     read_gbs = None
     try:
+        if args.no_read_probe:
+            raise RuntimeError("read probe skipped")
         buf = torch.empty(4 << 30, dtype=torch.uint8, device="cuda").view(torch.int32)
         buf.fill_(1)
         for _ in range(3):

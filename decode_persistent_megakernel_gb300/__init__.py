@@ -17,13 +17,14 @@ TINFER_OK, TINFER_ERR_INVALID_ARG, TINFER_ERR_UNSUPPORTED, TINFER_ERR_CUDA, TINF
 TINFER_BF16, TINFER_INT4 = 0, 1
 TINFER_SCALE_FP16, TINFER_SCALE_BF16 = 0, 1
 TINFER_MEGAKERNEL, TINFER_GRAPH = 0, 1
-TINFER_Q_GRID, TINFER_Q_SMEM, TINFER_Q_RING_STAGES, TINFER_Q_SLOT_BYTES, TINFER_Q_KERNELS_PER_STEP = range(5)
+TINFER_Q_GRID, TINFER_Q_SMEM, TINFER_Q_RING_STAGES, TINFER_Q_SLOT_BYTES, TINFER_Q_KERNELS_PER_STEP, \
+    TINFER_Q_TRACE_BYTES = range(6)
 TINFER_EPI_STORE, TINFER_EPI_RESIDUAL, TINFER_EPI_SWIGLU, TINFER_EPI_ARGMAX = range(4)
 
 EXPORTS = [
     "tinfer_status_string", "tinfer_check_config", "tinfer_packed_layer_bytes", "tinfer_pack_layer",
     "tinfer_unpack_layer", "tinfer_create", "tinfer_decode_step", "tinfer_decode_step_dev",
-    "tinfer_generate", "tinfer_get_error", "tinfer_query", "tinfer_set_timeout_ns",
+    "tinfer_generate", "tinfer_get_error", "tinfer_query", "tinfer_set_trace", "tinfer_set_timeout_ns",
     "tinfer_debug_skip_barrier", "tinfer_destroy", "tinfer_packed_row_bytes", "tinfer_pack_matrix",
     "tinfer_op_gemv", "tinfer_op_attention",
 ]
@@ -83,6 +84,7 @@ def lib():
             "tinfer_generate": ([P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P, P], I),
             "tinfer_get_error": ([P], I),
             "tinfer_query": ([P, I], LL),
+            "tinfer_set_trace": ([P, P], I),
             "tinfer_set_timeout_ns": ([P, LL], I),
             "tinfer_debug_skip_barrier": ([P, I, I], I),
             "tinfer_destroy": ([P], None),
@@ -174,6 +176,10 @@ def tinfer_get_error(ctx) -> int:
 
 def tinfer_query(ctx, what: int) -> int:
     return lib().tinfer_query(ctx, what)
+
+
+def tinfer_set_trace(ctx, trace_dev) -> int:
+    return lib().tinfer_set_trace(ctx, _ptr(trace_dev))
 
 
 def tinfer_set_timeout_ns(ctx, ns: int) -> int:
@@ -305,6 +311,20 @@ class Engine:
         rc = tinfer_decode_step_dev(self.ctx, token_dev, pos, stream, self.logits if logits else None,
                                     self.argmax if argmax is None else argmax)
         _check(rc, "tinfer_decode_step_dev")
+
+    def trace_step(self, token: int, pos: int):
+        """Runs one traced megakernel step; returns int64 stamps [grid][phases][6] (ns, relative to
+        the earliest stamp)."""
+        import numpy as np
+        import torch
+        nbytes = self.query(TINFER_Q_TRACE_BYTES)
+        buf = torch.zeros(nbytes // 8, dtype=torch.int64, device=self.device)
+        _check(tinfer_set_trace(self.ctx, buf), "tinfer_set_trace")
+        self.step(token, pos)
+        torch.cuda.synchronize()
+        _check(tinfer_set_trace(self.ctx, None), "tinfer_set_trace")
+        t = buf.cpu().numpy().reshape(self.query(TINFER_Q_GRID), -1, 6)
+        return t - t[t > 0].min()
 
     def error(self) -> int:
         return tinfer_get_error(self.ctx)

@@ -46,6 +46,15 @@ int max_row_bytes(const tinfer_config* c) {
   return (int)m;
 }
 
+// bytes of the shared-memory copy of the widest GEMV input vector (fp32 hidden, attention output or
+// SwiGLU output)
+int xs_bytes_for(const tinfer_config* c) {
+  int n = c->hidden;
+  if (c->n_heads * c->head_dim > n) n = c->n_heads * c->head_dim;
+  if (c->ffn > n) n = c->ffn;
+  return (int)align_up((size_t)n * 4, 128);
+}
+
 int slot_bytes_for(const tinfer_config* c) {
   const int m = max_row_bytes(c);
   return m <= SLOT_MIN ? SLOT_MIN : (int)align_up((size_t)m, 1024);
@@ -80,10 +89,9 @@ struct tinfer_ctx {
   int num_sms = 0;
   StepParams p{};
   int slot = 0;
-  int stages_mega = 0, stages_phase = 0;
+  int stages_mega = 0, stages_phase = 0, xs_bytes = 0;
   size_t smem_mega = 0, smem_phase = 0;
   void* scratch = nullptr;
-  LayerDev* layers_dev = nullptr;
   float2* rope_dev = nullptr;
   int* err_host = nullptr;     // mapped pinned
   int* err_host_dev = nullptr;
@@ -128,6 +136,7 @@ tinfer_status tinfer_check_config(const tinfer_config* c) {
   if (!(c->rope_theta > 0.0) || !(c->rms_eps >= 0.0)) return TINFER_ERR_INVALID_ARG;
   if (c->n_heads % c->n_kv_heads != 0 || c->head_dim % 2 != 0) return TINFER_ERR_INVALID_ARG;
   if (c->exec_mode != TINFER_MEGAKERNEL && c->exec_mode != TINFER_GRAPH) return TINFER_ERR_INVALID_ARG;
+  if (c->n_layers > MAX_LAYERS) return TINFER_ERR_UNSUPPORTED;
   if (c->weight_format != TINFER_BF16 && c->weight_format != TINFER_INT4) return TINFER_ERR_INVALID_ARG;
   if (c->n_heads / c->n_kv_heads > G_MAX || c->head_dim % 8 != 0 || c->head_dim > D_MAX)
     return TINFER_ERR_UNSUPPORTED;
@@ -135,13 +144,13 @@ tinfer_status tinfer_check_config(const tinfer_config* c) {
   const int widths[3] = {c->hidden, qd, c->ffn};
   for (int w : widths) {
     if (packed_row_bytes(c->weight_format, w, c->group_size) == 0) return TINFER_ERR_UNSUPPORTED;
-    if (c->weight_format == TINFER_INT4 && w / 32 > NCT) return TINFER_ERR_UNSUPPORTED;
-    if (c->weight_format == TINFER_BF16 && w / 8 > 5 * NCT) return TINFER_ERR_UNSUPPORTED;
+    if (!seg_ok(c->weight_format, w)) return TINFER_ERR_UNSUPPORTED;
   }
   if (c->weight_format == TINFER_INT4 && c->scale_dtype != TINFER_SCALE_FP16 &&
       c->scale_dtype != TINFER_SCALE_BF16)
     return TINFER_ERR_INVALID_ARG;
-  if (c->hidden % 8 != 0 || c->hidden / 8 > 5 * NCT) return TINFER_ERR_UNSUPPORTED;  // LM head
+  if (c->hidden % 8 != 0 || !seg_ok(TINFER_BF16, c->hidden)) return TINFER_ERR_UNSUPPORTED;  // LM head
+  if ((size_t)c->hidden * 4 > (size_t)slot_bytes_for(c)) return TINFER_ERR_UNSUPPORTED;  // gain stage
   const int slot = slot_bytes_for(c);
   int tmax = slot / (2 * c->head_dim);
   if (tmax > T_MAX) tmax = T_MAX;
@@ -263,7 +272,6 @@ static void free_ctx(tinfer_ctx* x) {
   if (x->graph) cudaGraphDestroy(x->graph);
   if (x->cap_stream) cudaStreamDestroy(x->cap_stream);
   if (x->scratch) cudaFree(x->scratch);
-  if (x->layers_dev) cudaFree(x->layers_dev);
   if (x->rope_dev) cudaFree(x->rope_dev);
   if (x->err_host) cudaFreeHost(x->err_host);
   if (x->pinned) cudaFreeHost(x->pinned);
@@ -276,6 +284,8 @@ tinfer_status tinfer_create(const tinfer_config* c, const tinfer_weights* w, voi
   *out = nullptr;
   TRY(tinfer_check_config(c));
   if (!w || !w->embed || !w->lm_head || !w->final_norm || !w->layer_blobs || !k_cache_dev || !v_cache_dev)
+    return TINFER_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(w->embed) & 15) != 0 || (reinterpret_cast<uintptr_t>(w->final_norm) & 7) != 0)
     return TINFER_ERR_INVALID_ARG;
   for (int l = 0; l < c->n_layers; ++l)
     if (!w->layer_blobs[l] || (reinterpret_cast<uintptr_t>(w->layer_blobs[l]) & 15) != 0)
@@ -300,20 +310,38 @@ tinfer_status tinfer_create(const tinfer_config* c, const tinfer_weights* w, voi
   if ((st = cu(cudaDeviceGetAttribute(&smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, x->device))) != TINFER_OK) return fail(st);
 
   x->slot = slot_bytes_for(c);
-  const size_t misc = smem_for(0, 0);
+  x->xs_bytes = xs_bytes_for(c);
+  const size_t misc = smem_for(0, 0, x->xs_bytes);
   x->stages_mega = (int)((smem_optin - misc) / x->slot);
   if (x->stages_mega > 8) x->stages_mega = 8;
+  while (x->stages_mega > 2 && smem_for(x->stages_mega, x->slot, x->xs_bytes) > (size_t)smem_optin) --x->stages_mega;
   // two CTAs of the per-phase kernel per SM, so that the next kernel's prefetch overlaps
   x->stages_phase = (int)((smem_per_sm / 2 - 1024 - misc) / x->slot);
   if (x->stages_phase > 4) x->stages_phase = 4;
+  if (x->stages_phase < 2) x->stages_phase = x->stages_mega < 4 ? x->stages_mega : 4;
+  while (x->stages_phase > 2 && smem_for(x->stages_phase, x->slot, x->xs_bytes) > (size_t)smem_optin) --x->stages_phase;
   if (x->stages_mega < 2 || x->stages_phase < 2) return fail(TINFER_ERR_UNSUPPORTED);
-  x->smem_mega = smem_for(x->stages_mega, x->slot);
-  x->smem_phase = smem_for(x->stages_phase, x->slot);
-  if ((st = cu(set_smem_limits(x->smem_mega, x->smem_phase, smem_for(4, x->slot)))) != TINFER_OK) return fail(st);
+  x->smem_mega = smem_for(x->stages_mega, x->slot, x->xs_bytes);
+  x->smem_phase = smem_for(x->stages_phase, x->slot, x->xs_bytes);
+  if ((st = cu(set_smem_mega(x->smem_mega))) != TINFER_OK) return fail(st);
+  if ((st = cu(set_smem_phase(x->smem_phase))) != TINFER_OK) return fail(st);
   int occ = 0;
-  if ((st = cu(megakernel_occupancy(&occ, x->smem_mega))) != TINFER_OK) return fail(st);
+  if ((st = cu(megakernel_occupancy(&occ, x->smem_mega, c->weight_format))) != TINFER_OK) return fail(st);
   if (occ < 1) return fail(TINFER_ERR_UNSUPPORTED);
   const int grid = x->num_sms;  // one persistent CTA per SM (co-residency: cooperative launch)
+  {
+    // row results of one GEMV phase must fit the per-CTA shared-memory buffer
+    const int f = c->weight_format;
+    const int qd = c->n_heads * c->head_dim;
+    const int rows[4] = {(c->n_heads + 2 * c->n_kv_heads) * c->head_dim, c->hidden, 2 * c->ffn, c->hidden};
+    const int cols[4] = {c->hidden, qd, c->hidden, c->ffn};
+    for (int i = 0; i < 4; ++i)
+      if ((long long)((rows[i] + grid - 1) / grid + 1) * seg_info(f, cols[i]).nseg > ROWV_MAX)
+        return fail(TINFER_ERR_UNSUPPORTED);
+    const int lm_seg = seg_info(TINFER_BF16, c->hidden).nseg;  // LM rows wider than one segment
+    if (lm_seg > 1 && (long long)((c->vocab + grid - 1) / grid) * lm_seg > ROWV_MAX)
+      return fail(TINFER_ERR_UNSUPPORTED);
+  }
 
   const int H = c->hidden, nq = c->n_heads, nkv = c->n_kv_heads, d = c->head_dim, F = c->ffn;
   const int qkv_rows = (nq + 2 * nkv) * d;
@@ -326,7 +354,7 @@ tinfer_status tinfer_create(const tinfer_config* c, const tinfer_weights* w, voi
   const size_t o_attn = take((size_t)nq * d * 4), o_act = take((size_t)F * 4);
   const size_t o_pm = take((size_t)nq * nch_cap * 4), o_pl = take((size_t)nq * nch_cap * 4);
   const size_t o_po = take((size_t)nq * nch_cap * d * 4);
-  const size_t o_tk = take((size_t)(nkv + 1) * 4), o_gb = take(2 * 4);
+  const size_t o_tk = take((size_t)(nkv + 1) * 4), o_gb = take(4);
   const size_t o_bv = take((size_t)grid * 4), o_bi = take((size_t)grid * 4), o_bb = take((size_t)grid * 4);
   const size_t o_err = take(4), o_step = take(2 * 4), o_gen = take(2 * 4), o_am = take(4);
   if ((st = cu(cudaMalloc(&x->scratch, off))) != TINFER_OK) return fail(st);
@@ -337,6 +365,7 @@ tinfer_status tinfer_create(const tinfer_config* c, const tinfer_weights* w, voi
   // layers
   const LayerLayout LL = layer_layout(H, nq, nkv, d, F, c->weight_format, c->group_size, c->qkv_bias);
   std::vector<LayerDev> ld(c->n_layers);
+  if (c->n_layers > MAX_LAYERS) return fail(TINFER_ERR_UNSUPPORTED);
   for (int l = 0; l < c->n_layers; ++l) {
     const uint8_t* b = (const uint8_t*)w->layer_blobs[l];
     ld[l].qkv = b + LL.off_qkv; ld[l].o = b + LL.off_o; ld[l].gu = b + LL.off_gu;
@@ -344,8 +373,6 @@ tinfer_status tinfer_create(const tinfer_config* c, const tinfer_weights* w, voi
     ld[l].g2 = (const float*)(b + LL.off_g2);
     ld[l].bias = c->qkv_bias ? (const float*)(b + LL.off_bias) : nullptr;
   }
-  if ((st = cu(cudaMalloc(&x->layers_dev, sizeof(LayerDev) * ld.size()))) != TINFER_OK) return fail(st);
-  if ((st = cu(cudaMemcpy(x->layers_dev, ld.data(), sizeof(LayerDev) * ld.size(), cudaMemcpyHostToDevice))) != TINFER_OK) return fail(st);
 
   std::vector<float2> rt;
   rope_table(rt, c->max_ctx, d, c->rope_theta);
@@ -367,7 +394,7 @@ tinfer_status tinfer_create(const tinfer_config* c, const tinfer_weights* w, voi
   m.rb_f = (int)packed_row_bytes(m.fmt, F, m.group);
   m.rb_lm = H * 2;
   m.qkv_rows = qkv_rows;
-  p.layers = x->layers_dev;
+  for (int l = 0; l < c->n_layers; ++l) p.layers[l] = ld[l];
   p.embed = (const uint16_t*)w->embed;
   p.lm_head = (const uint16_t*)w->lm_head;
   p.final_norm = (const uint16_t*)w->final_norm;
@@ -384,6 +411,8 @@ tinfer_status tinfer_create(const tinfer_config* c, const tinfer_weights* w, voi
   p.nch_cap = nch_cap;
   p.grid = grid;
   p.slot_bytes = x->slot;
+  p.inflight = 2;
+  p.bar_base = 0;
   p.timeout_ns = DEFAULT_TIMEOUT_NS;
   p.step_dev = (int*)(s + o_step);
   x->gen_dev = (int*)(s + o_gen);
@@ -391,6 +420,7 @@ tinfer_status tinfer_create(const tinfer_config* c, const tinfer_weights* w, voi
   p.n_chunks_override = 0;
   p.dbg_skip_cta = -1;
   p.dbg_skip_barrier = -1;
+  p.trace = nullptr;
   *out = x;
   return TINFER_OK;
 }
@@ -407,6 +437,7 @@ static tinfer_status build_graph(tinfer_ctx* x, float* logits, int* argmax) {
   p.token = 0; p.token_dev = nullptr; p.pos = 0;
   p.logits = logits; p.argmax = argmax;
   p.dbg_skip_cta = -1;
+  p.trace = nullptr;
   cudaStream_t cs = x->cap_stream;
   TRY_CUDA(cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal));
   cudaError_t e = launch_begin(const_cast<int*>(p.step_dev), 0, nullptr, 0, x->cfg.vocab, p.err, p.err_host, cs);
@@ -460,6 +491,7 @@ static tinfer_status step_impl(tinfer_ctx* x, int token, const int* token_dev, i
     p.logits = logits; p.argmax = argmax;
     TRY_CUDA(launch_megakernel(p, x->smem_mega, st));
     x->p.dbg_skip_cta = -1;  // an injected fault applies to one step only
+    x->p.bar_base += (unsigned)(x->cfg.n_layers * PHASES_PER_LAYER) * (unsigned)x->p.grid;
     return TINFER_OK;
   }
   if (!x->gexec || x->graph_logits != logits || x->graph_argmax != argmax)
@@ -489,7 +521,8 @@ tinfer_status tinfer_get_error(tinfer_ctx* x) {
   if (w || *reinterpret_cast<volatile int*>(x->err_host)) {
     uint8_t* s = (uint8_t*)x->scratch;
     TRY_CUDA(cudaMemset(s + x->err_off, 0, 4));
-    TRY_CUDA(cudaMemset(s + x->gbar_off, 0, 8));
+    TRY_CUDA(cudaMemset(s + x->gbar_off, 0, 4));
+    x->p.bar_base = 0;
     TRY_CUDA(cudaMemset(s + x->tickets_off, 0, (size_t)(x->cfg.n_kv_heads + 1) * 4));
     TRY_CUDA(cudaDeviceSynchronize());
     *reinterpret_cast<volatile int*>(x->err_host) = 0;
@@ -526,8 +559,17 @@ long long tinfer_query(const tinfer_ctx* x, int what) {
     case TINFER_Q_SLOT_BYTES: return x->slot;
     case TINFER_Q_KERNELS_PER_STEP:
       return x->cfg.exec_mode == TINFER_MEGAKERNEL ? 1 : x->cfg.n_layers * PHASES_PER_LAYER + 2;
+    case TINFER_Q_TRACE_BYTES:
+      return (long long)x->p.grid * (x->cfg.n_layers * PHASES_PER_LAYER + 1) * TRACE_FIELDS * 8;
   }
   return -1;
+}
+
+tinfer_status tinfer_set_trace(tinfer_ctx* x, void* trace_dev) {
+  if (!x) return TINFER_ERR_INVALID_ARG;
+  if (trace_dev && (reinterpret_cast<uintptr_t>(trace_dev) & 7) != 0) return TINFER_ERR_INVALID_ARG;
+  x->p.trace = (unsigned long long*)trace_dev;
+  return TINFER_OK;
 }
 
 tinfer_status tinfer_set_timeout_ns(tinfer_ctx* x, long long ns) {
@@ -593,14 +635,17 @@ tinfer_status tinfer_op_gemv(int fmt, int group, int scale_dtype, int rows, int 
   if (epilogue != TINFER_EPI_ARGMAX && !y_dev) return TINFER_ERR_INVALID_ARG;
   if (epilogue == TINFER_EPI_ARGMAX && !argmax_dev) return TINFER_ERR_INVALID_ARG;
   if (epilogue == TINFER_EPI_SWIGLU && rows % 2) return TINFER_ERR_INVALID_ARG;
-  if ((fmt == TINFER_INT4 && cols / 32 > NCT) || (fmt == TINFER_BF16 && cols / 8 > 5 * NCT))
-    return TINFER_ERR_UNSUPPORTED;
+  if (!seg_ok(fmt, cols)) return TINFER_ERR_UNSUPPORTED;
+  if (gain_dev && (reinterpret_cast<uintptr_t>(gain_dev) & 15) != 0) return TINFER_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(packed_dev) & 15) != 0) return TINFER_ERR_INVALID_ARG;
   TRY(op_scratch());
-  const int slot = rb * 2 <= SLOT_MIN ? SLOT_MIN : (int)align_up(rb * 2, 1024);
+  size_t need_slot = std::max(rb * 2, gain_dev ? (size_t)cols * 4 : (size_t)0);
+  const int slot = need_slot <= SLOT_MIN ? SLOT_MIN : (int)align_up(need_slot, 1024);
   const int stages = 4;
-  const size_t smem = smem_for(stages, slot);
-  TRY_CUDA(set_smem_limits(smem_for(2, slot), smem_for(2, slot), smem));
+  const int xs = (int)align_up((size_t)cols * 4, 128);
+  const size_t smem = smem_for(stages, slot, xs);
+  if (smem > 227 * 1024) return TINFER_ERR_UNSUPPORTED;
+  TRY_CUDA(set_smem_op_gemv(smem));
   OpGemvParams q{};
   q.w = (const uint8_t*)packed_dev; q.rows = rows; q.cols = cols; q.rb = (int)rb;
   q.fmt = fmt; q.group = group; q.scale_bf16 = scale_dtype == TINFER_SCALE_BF16;
@@ -609,7 +654,15 @@ tinfer_status tinfer_op_gemv(int fmt, int group, int scale_dtype, int rows, int 
   q.slot_v = g_op.slot_v; q.slot_i = g_op.slot_i; q.slot_bad = g_op.slot_bad; q.ticket = g_op.ticket;
   q.err = g_op.err; q.stages = stages; q.slot = slot; q.timeout_ns = DEFAULT_TIMEOUT_NS;
   const int quantum = epilogue == TINFER_EPI_SWIGLU ? 2 : 1;
-  const int grid = op_grid(rows / quantum);
+  int grid = op_grid(rows / quantum);
+  if (epilogue != TINFER_EPI_ARGMAX || seg_info(fmt, cols).nseg > 1) {
+    // enough CTAs that each one's row results fit its shared-memory buffer
+    const int nseg = seg_info(fmt, cols).nseg;
+    const int per = ROWV_MAX / nseg - quantum;
+    const int need = (rows + per - 1) / per;
+    if (need > grid) grid = need;
+  }
+  if (epilogue == TINFER_EPI_ARGMAX && grid > 1024) return TINFER_ERR_UNSUPPORTED;  // argmax slots
   cudaStream_t st = (cudaStream_t)stream;
   TRY_CUDA(launch_op_gemv(q, grid, smem, st));
   if (epilogue == TINFER_EPI_ARGMAX) {
@@ -667,8 +720,8 @@ tinfer_status tinfer_op_attention(int nq, int nkv, int d, int max_ctx, double th
     q.nch_cap = nch; q.tickets = tickets; q.out = out_dev;
     q.nq = nq; q.nkv = nkv; q.d = d; q.max_ctx = max_ctx; q.pos = pos; q.n_chunks = nch;
     q.err = g_op.err; q.stages = 4; q.slot = slot; q.timeout_ns = DEFAULT_TIMEOUT_NS;
-    const size_t smem = smem_for(4, slot);
-    if ((rc = from_cuda(set_smem_limits(smem_for(2, slot), smem_for(2, slot), smem))) != TINFER_OK) break;
+    const size_t smem = smem_for(4, slot, 0);
+    if ((rc = from_cuda(set_smem_op_attention(smem))) != TINFER_OK) break;
     if ((rc = from_cuda(launch_op_attention(q, grid, smem, st))) != TINFER_OK) break;
     if ((rc = from_cuda(cudaStreamSynchronize(st))) != TINFER_OK) break;
     int w = 0;

@@ -10,10 +10,20 @@ namespace tinfer {
 constexpr int NCW = 8;
 constexpr int NCT = NCW * 32;
 constexpr int NTHREADS = NCT + 32;
+// The persistent kernel runs a 4-warp producer group instead of one producer warp, so that the two
+// groups can trade registers (setmaxnreg): the producer group keeps REG_PRODUCER registers per
+// thread, the consumer warps grow to REG_CONSUMER. Launch total: 12 warps x 32 x 168 = 64512 =
+// 8 x 32 x REG_CONSUMER + 4 x 32 x REG_PRODUCER.
+constexpr int NTHREADS_MEGA = NCT + 128;
+constexpr int REG_CONSUMER = 232;
+constexpr int REG_PRODUCER = 40;
+static_assert(NCW * 32 * REG_CONSUMER + 4 * 32 * REG_PRODUCER <= (NTHREADS_MEGA / 32) * 32 * 168,
+              "register split exceeds the launch allocation");
 constexpr int NR_MAX = 32;    // rows of one matrix held by one ring stage, at most
 constexpr int G_MAX = 8;      // query heads sharing one KV head, at most
 constexpr int D_MAX = 128;    // head_dim, at most
 constexpr int T_MAX = 256;    // cache slots in one attention chunk, at most
+constexpr int MAX_LAYERS = 64;   // layer descriptors travel in the kernel parameters
 
 enum Phase : int { PH_QKV = 0, PH_ATTN = 1, PH_O = 2, PH_GU = 3, PH_DOWN = 4, PH_LM = 5 };
 constexpr int PHASES_PER_LAYER = 5;
@@ -49,7 +59,7 @@ struct Dims {
 // Everything one step needs; passed by value to every kernel.
 struct StepParams {
   Dims m;
-  const LayerDev* layers;
+  LayerDev layers[MAX_LAYERS];  // read through the constant cache
   const uint16_t* embed;
   const uint16_t* lm_head;
   const uint16_t* final_norm;
@@ -64,7 +74,8 @@ struct StepParams {
   float* part_l;           // [nq][nch_cap]
   float* part_o;           // [nq][nch_cap][d]
   unsigned* tickets;       // [nkv + 1]: attention merge per KV head, then the argmax ticket
-  unsigned* gbar;          // [2]: grid barrier arrival count and generation
+  unsigned* gbar;          // [1]: grid barrier arrival counter (monotonic; wraps)
+  unsigned bar_base;       // counter value at the start of this launch
   float* best_val;         // [grid]
   int* best_idx;           // [grid]
   int* best_bad;           // [grid]
@@ -74,6 +85,7 @@ struct StepParams {
   int grid;                // CTAs
   int ring_stages;
   int slot_bytes;
+  int inflight;            // bulk copies the producer keeps outstanding at most
   long long timeout_ns;
   // per step
   int token;               // used when token_dev is null
@@ -85,6 +97,18 @@ struct StepParams {
   int* argmax;             // [1]
   int dbg_skip_cta;        // fault injection: CTA that skips one grid-barrier arrival (-1 none)
   int dbg_skip_barrier;
+  unsigned long long* trace;  // optional timeline [grid][phases][TRACE_FIELDS] of %globaltimer ns
+};
+
+// Timeline fields recorded per CTA and phase when StepParams::trace is set.
+enum TraceField : int {
+  TR_START = 0,      // consumers begin the phase (after the previous grid barrier)
+  TR_READY = 1,      // activations loaded (norm done): the stage loop starts
+  TR_END = 2,        // consumers done with the phase (before the grid barrier)
+  TR_PROD_BEGIN = 3, // producer starts issuing the phase's copies
+  TR_PROD_END = 4,   // producer has issued the phase's last copy
+  TR_ACT = 5,        // the phase's input activations have arrived (before the norm)
+  TRACE_FIELDS = 6
 };
 
 // Op-level GEMV description (the single-operation entry point uses the same device code).
@@ -102,6 +126,46 @@ struct GemvOp {
 };
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+#ifdef __CUDACC__
+#define TINFER_HD __host__ __device__
+#else
+#define TINFER_HD
+#endif
+
+constexpr int SEG_MAX_INPUTS = 2048;  // inputs of one row segment (activations held per lane: 64)
+constexpr int ROWV_MAX = 1024;        // row results of one phase kept in shared memory per CTA
+
+// GEMV row segmenting: a row of `cols` inputs is cut into nseg (a power of two, at most NCW)
+// contiguous segments of ks inputs, chs 16-byte chunks each. A warp owns one segment of a row; the
+// activations of that segment stay in its lanes' registers (chunk c = lane + 32 k).
+struct SegInfo {
+  int nseg, ks, chs;
+};
+TINFER_HD inline SegInfo seg_info(int fmt, int cols) {
+  const int E = fmt ? 32 : 8;
+  int nseg = 1;
+  while (cols / nseg > SEG_MAX_INPUTS && nseg < NCW) nseg *= 2;
+  return SegInfo{nseg, cols / nseg, cols / nseg / E};
+}
+// True when the segmenting covers the row exactly and fits the per-lane register budget.
+TINFER_HD inline bool seg_ok(int fmt, int cols) {
+  const int E = fmt ? 32 : 8;
+  const SegInfo s = seg_info(fmt, cols);
+  return cols % s.nseg == 0 && s.ks % E == 0 && s.ks <= SEG_MAX_INPUTS && (s.chs + 31) / 32 <= 8;
+}
+// Rows of one ring stage: as many as fit a slot, rounded down to a multiple of the warps that
+// share a stage (NCW / nseg) and of the row quantum (2 for gate/up pairs), at least one quantum.
+TINFER_HD inline int stage_rows(int fmt, int cols, int rb, int slot, int quantum) {
+  const SegInfo s = seg_info(fmt, cols);
+  int wg = NCW / s.nseg;
+  int step = wg % quantum == 0 ? wg : wg * quantum;
+  int fit = slot / rb;
+  if (fit > NR_MAX) fit = NR_MAX;
+  int nr = fit - fit % step;
+  if (nr == 0) nr = fit - fit % quantum;
+  return nr;
+}
 
 // Packed row bytes: bf16 rows are 2*cols (cols % 8 == 0); int4 rows are cols/2 nibble bytes plus
 // 2*cols/group scale bytes, padded to 16 (cols % 32 == 0, group % 32 == 0, cols % group == 0).

@@ -74,19 +74,40 @@ __device__ void produce_phase(const StepParams& p, Pipe& pp, int phase, int laye
     return;
   }
   const GemvDesc g = phase_gemv(p, phase, layer);
-  produce_rows(pp, g, row_split(g, blockIdx.x, p.grid, p.slot_bytes), pol_w, dead);
+  const void* gain = nullptr;
+  uint32_t gain_bytes = 0;
+  if (phase == PH_QKV) { gain = p.layers[layer].g1; gain_bytes = p.m.H * 4; }
+  else if (phase == PH_GU) { gain = p.layers[layer].g2; gain_bytes = p.m.H * 4; }
+  else if (phase == PH_LM) { gain = p.final_norm; gain_bytes = p.m.H * 2; }
+  produce_rows(pp, g, row_split(g, blockIdx.x, p.grid, p.slot_bytes), pol_w, dead, gain, gain_bytes);
 }
 
-__device__ void consume_phase(const StepParams& p, Pipe& pp, int phase, int layer, int token,
-                              int pos, int tid) {
+__device__ __forceinline__ unsigned long long* trace_at(const StepParams& p, int k, int field) {
+  if (!p.trace) return nullptr;
+  const int nph = p.m.L * PHASES_PER_LAYER + 1;
+  return p.trace + ((size_t)blockIdx.x * nph + k) * TRACE_FIELDS + field;
+}
+
+// Consumer side of one attention phase (every unit this CTA owns). Separate from the GEMV phase so
+// that each gets its own register allocation; the pipe state goes in and comes back by value.
+__device__ __forceinline__ Pipe consume_attn_phase(const StepParams& p, Pipe pp, int layer, int pos,
+                                                int tid, int k) {
+  unsigned long long* tr_ready = trace_at(p, k, TR_READY);
+  if (tr_ready && tid == 0) *tr_ready = globaltimer();
+  const AttnArgs A = step_attn_args(p, layer, pos);
+  const AttnSplit sp = attn_split(pos, A.nkv, A.d, p.grid, p.slot_bytes, p.n_chunks_override);
+  const int units = A.nkv * sp.nch;
+  for (int u = blockIdx.x; u < units; u += p.grid) attn_unit(pp, A, sp, u / sp.nch, u % sp.nch, tid);
+  return pp;
+}
+
+// Consumer side of one GEMV phase: QKV (RMSNorm prologue, bias), O (+ residual), gate/up (RMSNorm,
+// SwiGLU), down (+ residual) or the LM head (final RMSNorm, logits, argmax).
+template <int FMT>
+__device__ __forceinline__ Pipe consume_gemv_phase(const StepParams& p, Pipe pp, int phase, int layer,
+                                                int token, int tid, int k) {
   const Dims& m = p.m;
-  if (phase == PH_ATTN) {
-    const AttnArgs A = step_attn_args(p, layer, pos);
-    const AttnSplit sp = attn_split(pos, A.nkv, A.d, p.grid, p.slot_bytes, p.n_chunks_override);
-    const int units = A.nkv * sp.nch;
-    for (int u = blockIdx.x; u < units; u += p.grid) attn_unit(pp, A, sp, u / sp.nch, u % sp.nch, tid);
-    return;
-  }
+  unsigned long long* tr_ready = trace_at(p, k, TR_READY);
   const GemvDesc g = phase_gemv(p, phase, layer);
   const RowSplit rs = row_split(g, blockIdx.x, p.grid, p.slot_bytes);
   const LayerDev& L = p.layers[layer];
@@ -117,7 +138,9 @@ __device__ void consume_phase(const StepParams& p, Pipe& pp, int phase, int laye
       break;
   }
   Best best{-CUDART_INF_F, 0x7FFFFFFF, 0};
-  gemv_consume_any(pp, g, rs, src, epi, best, tid);
+  // int4 models stream their linears as int4 and the LM head as bf16; bf16 models need one instance
+  if (FMT == 1 && g.fmt == 1) gemv_rows<1, 2>(pp, g, rs, src, epi, best, tid, tr_ready);
+  else gemv_rows<0, 8>(pp, g, rs, src, epi, best, tid, tr_ready);
   if (phase == PH_QKV && layer == 0 && blockIdx.x == 0)
     for (int i = tid; i < m.H; i += NCT) p.x[i] = bf16_to_f(p.embed[(size_t)token * m.H + i]);
   if (phase == PH_LM) {
@@ -125,38 +148,39 @@ __device__ void consume_phase(const StepParams& p, Pipe& pp, int phase, int laye
     argmax_publish(cb, p.best_val, p.best_idx, p.best_bad, p.tickets + m.nkv, p.grid, blockIdx.x,
                    p.argmax, p.err, p.err_host, pp.ms, tid);
   }
+  return pp;
 }
 
-// Sense-reversing barrier over the CTAs of the cooperative launch, run by the consumer warps.
-// Thread 0 arrives (after a fence that publishes the CTA's writes) and spins on the generation word
-// with a time limit; the spin also ends when another CTA has raised an error. Returns false, the
-// same in every consumer thread, when the step must stop.
+template <int FMT>
+__device__ __forceinline__ void consume_phase(const StepParams& p, Pipe& pp, int phase, int layer,
+                                              int token, int pos, int tid, int k) {
+  if (phase == PH_ATTN) pp = consume_attn_phase(p, pp, layer, pos, tid, k);
+  else pp = consume_gemv_phase<FMT>(p, pp, phase, layer, token, tid, k);
+}
+
+// Barrier over the CTAs of the cooperative launch, run by the consumer warps: one monotonic
+// arrival counter (it never resets; barrier k of a launch waits for bar_base + (k+1) * grid).
+// Thread 0 arrives with a release reduction that publishes the CTA's writes and polls with acquire
+// loads under a time limit; the poll also ends when another CTA has raised an error. Returns false,
+// the same in every consumer thread, when the step must stop.
 __device__ bool grid_sync(const StepParams& p, Misc* ms, int tid, int index) {
   named_sync(BAR_CONS, NCT);
   if (tid == 0) {
     int stop = *reinterpret_cast<volatile int*>(&ms->abort);
     const bool skip = (p.dbg_skip_cta == (int)blockIdx.x && p.dbg_skip_barrier == index);
     if (!stop && !skip) {
-      unsigned* cnt = p.gbar;
-      unsigned* gen = p.gbar + 1;
-      const unsigned g0 = ld_acquire(gen);
-      __threadfence();
-      const unsigned old = atomicAdd(cnt, 1u);
-      if (old == (unsigned)p.grid - 1) {
-        atomicExch(cnt, 0u);
-        __threadfence();
-        st_release(gen, g0 + 1);
-      } else {
-        const uint64_t t0 = globaltimer();
-        unsigned spins = 0;
-        while (ld_acquire(gen) == g0) {
-          if ((++spins & 63u) == 0) {
-            if (ld_volatile_int(p.err) != 0) { stop = 1; break; }
-            if ((long long)(globaltimer() - t0) > p.timeout_ns) {
-              raise_error(p.err, p.err_host, EW_TIMEOUT);
-              stop = 1;
-              break;
-            }
+      // barrier `index` of this launch completes when the counter reaches its target
+      const unsigned target = p.bar_base + (unsigned)(index + 1) * (unsigned)p.grid;
+      red_add_release(p.gbar, 1u);
+      const uint64_t t0 = globaltimer();
+      unsigned spins = 0;
+      while ((int)(ld_acquire(p.gbar) - target) < 0) {
+        if ((++spins & 63u) == 0) {
+          if (ld_volatile_int(p.err) != 0) { stop = 1; break; }
+          if ((long long)(globaltimer() - t0) > p.timeout_ns) {
+            raise_error(p.err, p.err_host, EW_TIMEOUT);
+            stop = 1;
+            break;
           }
         }
       }
@@ -186,11 +210,13 @@ __device__ __forceinline__ bool step_prologue(const StepParams& p, int& token, i
   return s_tok[1] == 0;
 }
 
-__global__ void __launch_bounds__(NTHREADS, 1) decode_megakernel(const __grid_constant__ StepParams p) {
+template <int FMT>
+__global__ void __launch_bounds__(NTHREADS_MEGA, 1) decode_megakernel(const __grid_constant__ StepParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ int s_tok[2];
   Pipe pp;
   pipe_init(pp, smem, p.ring_stages, p.slot_bytes, p.timeout_ns, p.err, p.err_host);
+  pp.inflight = p.inflight;
   pipe_setup(pp);
   int token = 0;
   const int pos = p.pos;
@@ -198,21 +224,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_megakernel(const __grid_co
   const int nph = p.m.L * PHASES_PER_LAYER + 1;
   const int tid = threadIdx.x;
   if (tid >= NCT) {
+    reg_dealloc<REG_PRODUCER>();
     if (tid == NCT) {
       const uint64_t pw = policy_evict_first(), pkv = policy_evict_normal();
       bool dead = false;
       for (int k = 0; k < nph && !dead; ++k) {
         int phase, layer;
         phase_of(k, p.m.L, phase, layer);
+        if (unsigned long long* t = trace_at(p, k, TR_PROD_BEGIN)) *t = globaltimer();
         produce_phase(p, pp, phase, layer, pos, pw, pkv, dead);
+        if (unsigned long long* t = trace_at(p, k, TR_PROD_END)) *t = globaltimer();
       }
       prod_drain(pp);
     }
   } else {
+    reg_alloc<REG_CONSUMER>();
     for (int k = 0; k < nph; ++k) {
       int phase, layer;
       phase_of(k, p.m.L, phase, layer);
-      consume_phase(p, pp, phase, layer, token, pos, tid);
+      if (unsigned long long* t = trace_at(p, k, TR_START)) if (tid == 0) *t = globaltimer();
+      consume_phase<FMT>(p, pp, phase, layer, token, pos, tid, k);
+      if (unsigned long long* t = trace_at(p, k, TR_END)) if (tid == 0) *t = globaltimer();
       if (k + 1 < nph && !grid_sync(p, pp.ms, tid, k)) break;
     }
     if (tid == 0) *reinterpret_cast<volatile int*>(&pp.ms->cons_done) = 1;
@@ -220,10 +252,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_megakernel(const __grid_co
   __syncthreads();
 }
 
+template <int FMT>
 __global__ void __launch_bounds__(NTHREADS, 2) decode_phase_kernel(const __grid_constant__ StepParams p, int k) {
   extern __shared__ __align__(128) unsigned char smem[];
   Pipe pp;
   pipe_init(pp, smem, p.ring_stages, p.slot_bytes, p.timeout_ns, p.err, p.err_host);
+  pp.inflight = p.inflight;
   pipe_setup(pp);
   __syncthreads();
   pdl_launch_dependents();
@@ -245,7 +279,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) decode_phase_kernel(const __grid_
     named_sync(BAR_CONS, NCT);
     if (!*reinterpret_cast<volatile int*>(&pp.ms->exit_now)) {
       const int token = p.step_dev[0], pos = p.step_dev[1];
-      consume_phase(p, pp, phase, layer, token, pos, tid);
+      consume_phase<FMT>(p, pp, phase, layer, token, pos, tid, k);
     }
     named_sync(BAR_CONS, NCT);
     if (tid == 0) *reinterpret_cast<volatile int*>(&pp.ms->cons_done) = 1;
@@ -275,7 +309,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) op_gemv_kernel(const __grid_const
   if (tid >= NCT) {
     if (tid == NCT) {
       bool dead = false;
-      produce_rows(pp, g, rs, policy_evict_first(), dead);
+      produce_rows(pp, g, rs, policy_evict_first(), dead, q.gain, q.gain ? (uint32_t)q.cols * 4u : 0u);
       prod_drain(pp);
     }
   } else {
@@ -283,7 +317,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) op_gemv_kernel(const __grid_const
     src.xf = q.x; src.gf = q.gain; src.eps = q.eps; src.n = q.cols;
     const Epi epi{q.epi, q.y, q.bias};
     Best best{-CUDART_INF_F, 0x7FFFFFFF, 0};
-    gemv_consume_any(pp, g, rs, src, epi, best, tid);
+    gemv_consume_any(pp, g, rs, src, epi, best, tid, nullptr);
     if (q.epi == EK_ARGMAX) {
       const Best cb = best_block_reduce(best, pp.ms, tid);
       argmax_publish(cb, q.slot_v, q.slot_i, q.slot_bad, q.ticket, gridDim.x, blockIdx.x, q.argmax,
@@ -365,10 +399,14 @@ __global__ void f32_to_bf16_kernel(const float* in, uint16_t* out, int n) {
 
 // ------------------------------------------------------------------------------ launch wrappers
 
+static const void* mega_fn(int fmt) {
+  return fmt == 1 ? reinterpret_cast<const void*>(&decode_megakernel<1>)
+                  : reinterpret_cast<const void*>(&decode_megakernel<0>);
+}
+
 cudaError_t launch_megakernel(const StepParams& p, size_t smem, cudaStream_t st) {
   void* args[] = {const_cast<StepParams*>(&p)};
-  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(&decode_megakernel), dim3(p.grid),
-                                     dim3(NTHREADS), args, smem, st);
+  return cudaLaunchCooperativeKernel(mega_fn(p.m.fmt), dim3(p.grid), dim3(NTHREADS_MEGA), args, smem, st);
 }
 
 cudaError_t launch_phase(const StepParams& p, int k, size_t smem, cudaStream_t st, bool pdl) {
@@ -382,7 +420,8 @@ cudaError_t launch_phase(const StepParams& p, int k, size_t smem, cudaStream_t s
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, decode_phase_kernel, p, k);
+  if (p.m.fmt == 1) return cudaLaunchKernelEx(&cfg, decode_phase_kernel<1>, p, k);
+  return cudaLaunchKernelEx(&cfg, decode_phase_kernel<0>, p, k);
 }
 
 cudaError_t launch_begin(int* step_dev, int token, const int* token_dev, int pos, int V, int* err,
@@ -403,24 +442,38 @@ cudaError_t launch_op_attention(const OpAttnParams& q, int grid, size_t smem, cu
   return cudaGetLastError();
 }
 
-cudaError_t set_smem_limits(size_t mega, size_t phase, size_t op) {
-  cudaError_t e = cudaFuncSetAttribute(decode_megakernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mega);
+// Raises (never lowers) a kernel's dynamic shared-memory limit; one limit per kernel and device.
+static cudaError_t raise_limit(const void* fn, int which, size_t bytes) {
+  static size_t cur[6][64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(decode_phase_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)phase);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(op_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)op);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(op_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)op);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (bytes <= cur[which][dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) cur[which][dev] = bytes;
+  return e;
+}
+cudaError_t set_smem_mega(size_t b) {
+  cudaError_t e = raise_limit((const void*)&decode_megakernel<0>, 0, b);
+  return e != cudaSuccess ? e : raise_limit((const void*)&decode_megakernel<1>, 4, b);
+}
+cudaError_t set_smem_phase(size_t b) {
+  cudaError_t e = raise_limit((const void*)&decode_phase_kernel<0>, 1, b);
+  return e != cudaSuccess ? e : raise_limit((const void*)&decode_phase_kernel<1>, 5, b);
+}
+cudaError_t set_smem_op_gemv(size_t b) { return raise_limit((const void*)op_gemv_kernel, 2, b); }
+cudaError_t set_smem_op_attention(size_t b) { return raise_limit((const void*)op_attention_kernel, 3, b); }
+
+cudaError_t megakernel_occupancy(int* blocks_per_sm, size_t smem, int fmt) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, mega_fn(fmt), NTHREADS_MEGA, smem);
+}
+cudaError_t phase_occupancy(int* blocks_per_sm, size_t smem, int fmt) {
+  if (fmt == 1) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_phase_kernel<1>, NTHREADS, smem);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_phase_kernel<0>, NTHREADS, smem);
 }
 
-cudaError_t megakernel_occupancy(int* blocks_per_sm, size_t smem) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_megakernel, NTHREADS, smem);
-}
-cudaError_t phase_occupancy(int* blocks_per_sm, size_t smem) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_phase_kernel, NTHREADS, smem);
-}
-
-size_t smem_for(int stages, int slot) { return step_smem_bytes(stages, slot); }
+size_t smem_for(int stages, int slot, int xs_bytes) { return step_smem_bytes(stages, slot, xs_bytes); }
 
 cudaError_t launch_pack_rows(uint8_t* dst, int dst_rb, int dst_step, int dst_first, int rows,
                              const uint8_t* w, int w_bytes, const uint8_t* s, int s_bytes,

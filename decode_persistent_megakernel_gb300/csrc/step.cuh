@@ -23,10 +23,10 @@ namespace tinfer {
 
 constexpr int MAX_STAGES = 8;
 
-struct Misc {
+struct __align__(16) Misc {
   unsigned long long full[MAX_STAGES];
   unsigned long long empty[MAX_STAGES];
-  float red[2][NR_MAX][NCW];   // per-stage cross-warp partial sums, double buffered
+  float rowv[ROWV_MAX];        // row results (per segment) of the current GEMV phase
   float wred[NCW];             // block-reduction scratch
   float qs[G_MAX * D_MAX];     // rotated, pre-scaled queries of the current attention unit
   float sc[G_MAX * T_MAX];     // scores, then probabilities; merge weights in the merge
@@ -43,19 +43,31 @@ struct Misc {
   int exit_now;   // uniform stop decision, written by consumer thread 0 between two named barriers
 };
 
-__host__ __device__ inline size_t step_smem_bytes(int stages, int slot_bytes) {
-  return (size_t)stages * slot_bytes + sizeof(Misc);
+// Dynamic shared memory: [ring: stages x slot][Misc][input vector: xs_bytes], every part starting
+// on a 128-byte boundary (bulk copies and 16-byte shared loads need 16).
+__host__ __device__ inline size_t misc_offset(int stages, int slot_bytes) {
+  return ((size_t)stages * slot_bytes + 127) / 128 * 128;
+}
+__host__ __device__ inline size_t xs_offset(int stages, int slot_bytes) {
+  return (misc_offset(stages, slot_bytes) + sizeof(Misc) + 127) / 128 * 128;
+}
+__host__ __device__ inline size_t step_smem_bytes(int stages, int slot_bytes, int xs_bytes) {
+  return xs_offset(stages, slot_bytes) + (size_t)xs_bytes;
 }
 
 constexpr int BAR_CONS = 1;  // named barrier id used by the consumer warps
 
 struct Pipe {
+  int inflight;     // producer: copies kept outstanding at most (0 = the whole ring)
   uint32_t ring;    // shared address of slot 0
   uint32_t full0;   // shared address of full[0]
   uint32_t empty0;  // shared address of empty[0]
   int stages;
   int slot;
   uint32_t it;      // stages issued (producer) or consumed (consumers)
+  int s;            // current slot
+  uint32_t ph;      // parity of the current slot's phase
+  uint32_t xs;      // shared address of the input-vector buffer
   Misc* ms;
   long long timeout;
   int* err;
@@ -69,7 +81,7 @@ __device__ __forceinline__ void raise_error(int* err, int* err_host, int bits) {
 
 // Waits until the phase of `parity` of mbarrier `bar` completes. Gives up after `timeout` ns, or as
 // soon as *stop is non-zero. Returns true on completion.
-__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, long long timeout,
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, long long timeout,
                                       const volatile int* stop) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
@@ -82,12 +94,17 @@ __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, long long t
   }
 }
 
+__device__ __forceinline__ void pipe_advance(Pipe& pp) {
+  ++pp.it;
+  if (++pp.s == pp.stages) { pp.s = 0; pp.ph ^= 1u; }
+}
+
 __device__ __forceinline__ uint32_t cons_acquire(Pipe& pp) {
-  const int s = pp.it % pp.stages;
-  const uint32_t par = (pp.it / pp.stages) & 1u;
+  const int s = pp.s;
+  if (mbar_try_wait(pp.full0 + 8u * s, pp.ph)) return pp.ring + (uint32_t)s * pp.slot;
   volatile int* ab = &pp.ms->abort;
   if (!*ab) {
-    if (!wait_bar(pp.full0 + 8u * s, par, pp.timeout, ab)) {
+    if (!wait_bar(pp.full0 + 8u * s, pp.ph, pp.timeout, ab)) {
       if (!*ab) {
         *ab = 1;
         raise_error(pp.err, pp.err_host, EW_TIMEOUT);
@@ -99,26 +116,36 @@ __device__ __forceinline__ uint32_t cons_acquire(Pipe& pp) {
 
 __device__ __forceinline__ void cons_release(Pipe& pp, int lane) {
   __syncwarp();
-  if (lane == 0) mbar_arrive(pp.empty0 + 8u * (pp.it % pp.stages));
-  ++pp.it;
+  if (lane == 0) mbar_arrive(pp.empty0 + 8u * pp.s);
+  pipe_advance(pp);
 }
 
 // Producer: one stage of `bytes` contiguous bytes (multiple of 16, <= slot) from src.
 __device__ __forceinline__ void prod_push(Pipe& pp, const void* src, uint32_t bytes, uint64_t pol,
                                           bool& dead) {
   if (dead) return;
-  const int s = pp.it % pp.stages;
-  const uint32_t par = ((pp.it / pp.stages) & 1u) ^ 1u;
-  if (!wait_bar(pp.empty0 + 8u * s, par, pp.timeout, &pp.ms->cons_done)) {
+  const int s = pp.s;
+  if (!wait_bar(pp.empty0 + 8u * s, pp.ph ^ 1u, pp.timeout, &pp.ms->cons_done)) {
     dead = true;
     if (!*reinterpret_cast<volatile int*>(&pp.ms->cons_done))
       raise_error(pp.err, pp.err_host, EW_TIMEOUT);
     return;
   }
+  if (pp.inflight > 0 && pp.it >= (uint32_t)pp.inflight) {
+    // bound the bytes in flight: the copy issued `inflight` stages ago must have landed
+    const int k = pp.inflight;
+    const int s2 = s >= k ? s - k : s - k + pp.stages;
+    const uint32_t p2 = s >= k ? pp.ph : pp.ph ^ 1u;
+    if (!mbar_try_wait(pp.full0 + 8u * s2, p2) &&
+        !wait_bar(pp.full0 + 8u * s2, p2, pp.timeout, &pp.ms->cons_done)) {
+      dead = true;
+      return;
+    }
+  }
   const uint32_t fb = pp.full0 + 8u * s;
   mbar_arrive_expect_tx(fb, bytes);
   if (bytes) bulk_g2s(pp.ring + (uint32_t)s * pp.slot, src, bytes, fb, pol);
-  ++pp.it;
+  pipe_advance(pp);
 }
 
 // Before the CTA exits: every copy this producer issued has landed (bounded wait).
@@ -129,15 +156,21 @@ __device__ void prod_drain(Pipe& pp) {
     wait_bar(pp.full0 + 8u * (k % pp.stages), (k / pp.stages) & 1u, pp.timeout, &never);
 }
 
+static_assert(sizeof(Misc) % 16 == 0, "Misc keeps 16-byte alignment");
+
 __device__ __forceinline__ void pipe_init(Pipe& pp, unsigned char* smem, int stages, int slot,
                                           long long timeout, int* err, int* err_host) {
   pp.ring = smem_addr(smem);
-  pp.ms = reinterpret_cast<Misc*>(smem + (size_t)stages * slot);
+  pp.ms = reinterpret_cast<Misc*>(smem + misc_offset(stages, slot));
   pp.full0 = smem_addr(&pp.ms->full[0]);
   pp.empty0 = smem_addr(&pp.ms->empty[0]);
+  pp.xs = smem_addr(smem + xs_offset(stages, slot));
   pp.stages = stages;
   pp.slot = slot;
+  pp.inflight = 0;
   pp.it = 0;
+  pp.s = 0;
+  pp.ph = 0;
   pp.timeout = timeout;
   pp.err = err;
   pp.err_host = err_host;
@@ -178,22 +211,10 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-// Block-wide sum over the consumer threads; every consumer thread gets the same value (fixed
-// summation order, so the result is bit-reproducible).
-__device__ __forceinline__ float cons_block_sum(float v, Misc* ms, int tid) {
-  v = warp_sum(v);
-  if ((tid & 31) == 0) ms->wred[tid >> 5] = v;
-  named_sync(BAR_CONS, NCT);
-  float t = 0.f;
-#pragma unroll
-  for (int w = 0; w < NCW; ++w) t += ms->wred[w];
-  named_sync(BAR_CONS, NCT);
-  return t;
-}
-
 // Reduces 8 per-lane partials (8 rows) across the 32 lanes with 9 shuffles. Afterwards lanes with
-// (lane & 3) == 0 hold the warp total of row ((lane>>4)&1)*4 + ((lane>>3)&1)*2 + ((lane>>2)&1).
-__device__ __forceinline__ float transpose_reduce8(float (&v)[8], int lane) {
+// (lane & 3) == 0 hold the warp total of row transpose_row8(lane). Every row's total is the same
+// summation tree, so identical rows give identical totals.
+__device__ __forceinline__ float transpose_reduce8(const float (&v)[8], int lane) {
   float a[4];
   {
     const bool up = lane & 16;
@@ -231,16 +252,13 @@ __device__ __forceinline__ int transpose_row8(int lane) {
 
 // ------------------------------------------------------------------------------ GEMV
 
-// 8 bf16 weights (one 16-byte chunk) dotted with 8 activations.
-__device__ __forceinline__ float dot8_bf16(const uint4 w, const float* a, float acc) {
-  acc = fmaf(bf16_lo(w.x), a[0], acc);
-  acc = fmaf(bf16_hi(w.x), a[1], acc);
-  acc = fmaf(bf16_lo(w.y), a[2], acc);
-  acc = fmaf(bf16_hi(w.y), a[3], acc);
-  acc = fmaf(bf16_lo(w.z), a[4], acc);
-  acc = fmaf(bf16_hi(w.z), a[5], acc);
-  acc = fmaf(bf16_lo(w.w), a[6], acc);
-  acc = fmaf(bf16_hi(w.w), a[7], acc);
+// 8 bf16 weights (one 16-byte chunk) times 8 activations, accumulated as (even, odd) pairs on the
+// packed f32x2 FMA units.
+__device__ __forceinline__ float2 dot8_bf16(const uint4 w, const float* a, float2 acc) {
+  acc = fma2(make_float2(bf16_lo(w.x), bf16_hi(w.x)), make_float2(a[0], a[1]), acc);
+  acc = fma2(make_float2(bf16_lo(w.y), bf16_hi(w.y)), make_float2(a[2], a[3]), acc);
+  acc = fma2(make_float2(bf16_lo(w.z), bf16_hi(w.z)), make_float2(a[4], a[5]), acc);
+  acc = fma2(make_float2(bf16_lo(w.w), bf16_hi(w.w)), make_float2(a[6], a[7]), acc);
   return acc;
 }
 
@@ -281,12 +299,6 @@ struct ActSrc {
   int n;
 };
 
-__device__ __forceinline__ float act_x(const ActSrc& s, int i) {
-  return s.xf ? __ldcg(s.xf + i) : bf16_to_f(s.xb[i]);
-}
-__device__ __forceinline__ float act_g(const ActSrc& s, int i) {
-  return s.gf ? s.gf[i] : bf16_to_f(s.gb[i]);
-}
 
 struct GemvDesc {
   const uint8_t* w;
@@ -303,10 +315,7 @@ __device__ __forceinline__ RowSplit row_split(const GemvDesc& g, int cta, int gr
   const int units = g.rows / g.quantum;
   const int u0 = (int)((long long)units * cta / grid);
   const int u1 = (int)((long long)units * (cta + 1) / grid);
-  int nr = slot / g.rb;
-  if (nr > NR_MAX) nr = NR_MAX;
-  nr -= nr % g.quantum;
-  return RowSplit{u0 * g.quantum, u1 * g.quantum, nr};
+  return RowSplit{u0 * g.quantum, u1 * g.quantum, stage_rows(g.fmt, g.cols, g.rb, slot, g.quantum)};
 }
 
 enum EpiKind : int { EK_STORE = 0, EK_RESIDUAL = 1, EK_SWIGLU = 2, EK_ARGMAX = 3 };
@@ -327,149 +336,253 @@ __device__ __forceinline__ void best_update(Best& b, float v, int i) {
   else if (v > b.v || (v == b.v && i < b.i)) { b.v = v; b.i = i; }
 }
 
-// Consumes one CTA's rows [rs.r0, rs.r1) of a matrix from the ring. Thread layout: a row is C
-// 16-byte chunks; when C >= NCT every thread owns chunks {t, t+NCT, ...} of every row (J of them);
-// otherwise the consumer threads split into RG row groups of ceil(C/32) warps, a group owning every
-// RG-th row of a stage and a thread one chunk. Activations of a thread's chunks stay in registers
-// for the whole matrix. Per stage: each thread forms its rows' partial dot products, the warp
-// transposes-and-reduces 8 rows at a time, the warps of a group meet in shared memory, and one
-// thread per row applies the epilogue. Every reduction has a fixed order.
-template <int FMT, int J>
-__device__ void gemv_consume(Pipe& pp, const GemvDesc& g, const RowSplit& rs, const ActSrc& src,
-                             const Epi& epi, Best& best, int tid) {
+// The phase's input vector, written by other CTAs before the last grid barrier, fetched once per
+// CTA into shared memory by all consumer threads together (16-byte loads through L2, batched four
+// deep): every warp of every CTA reading the same few cache lines serialises on those lines, one
+// read per CTA does not, and the load path does not queue behind the CTA's own bulk weight copies.
+// Called by all consumer threads; returns after the named barrier that publishes the copy.
+__device__ __forceinline__ void fetch_vector(Pipe& pp, const void* src, uint32_t bytes, int tid) {
+  const uint4* g = reinterpret_cast<const uint4*>(src);
+  const int n16 = (int)(bytes / 16u);
+  for (int i0 = tid; i0 < n16; i0 += 4 * NCT) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * NCT;
+      if (i < n16) v[u] = __ldcg(g + i);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * NCT;
+      if (i < n16)
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(pp.xs + (uint32_t)i * 16u),
+                     "r"(v[u].x), "r"(v[u].y), "r"(v[u].z), "r"(v[u].w)
+                     : "memory");
+    }
+  }
+  named_sync(BAR_CONS, NCT);
+}
+// 8 consecutive activations from the shared-memory vector (fp32 or bf16 source), index i % 8 == 0
+__device__ __forceinline__ void vec8(const Pipe& pp, bool f32, int i, float* o) {
+  if (f32) {
+    const uint4 u = lds128(pp.xs + (uint32_t)i * 4u), w = lds128(pp.xs + (uint32_t)i * 4u + 16u);
+    o[0] = __uint_as_float(u.x); o[1] = __uint_as_float(u.y); o[2] = __uint_as_float(u.z); o[3] = __uint_as_float(u.w);
+    o[4] = __uint_as_float(w.x); o[5] = __uint_as_float(w.y); o[6] = __uint_as_float(w.z); o[7] = __uint_as_float(w.w);
+  } else {
+    const uint4 b = lds128(pp.xs + (uint32_t)i * 2u);
+    o[0] = bf16_lo(b.x); o[1] = bf16_hi(b.x); o[2] = bf16_lo(b.y); o[3] = bf16_hi(b.y);
+    o[4] = bf16_lo(b.z); o[5] = bf16_hi(b.z); o[6] = bf16_lo(b.w); o[7] = bf16_hi(b.w);
+  }
+}
+
+// Consumes one CTA's rows [rs.r0, rs.r1) of a matrix from the ring ("How I built an LLM inference
+// engine from scratch in CUDA", v0.1 and "Round 1": a warp per row, 16-byte lane loads, several
+// rows per warp; here the rows come from the shared-memory ring instead of global memory).
+// A row is cut into nseg segments (seg_info); warp w owns segment w % nseg of rows
+// w / nseg, w / nseg + NCW / nseg, ... of every stage, and keeps that segment's activations in
+// registers for the whole matrix (lane owns chunks lane + 32 k). Per row: a warp dot product and a
+// butterfly reduction. The LM head applies its epilogue in the warp; every other matrix leaves its
+// per-segment row results in shared memory, and one pass at the end of the phase sums the
+// segments in a fixed order and applies the epilogue (bias, residual add, SwiGLU on gate/up pairs).
+template <int FMT, int NCHL>
+__device__ void gemv_rows(Pipe& pp, const GemvDesc& g, const RowSplit& rs, const ActSrc& src,
+                          const Epi& epi, Best& best, int tid, unsigned long long* tr_ready) {
   constexpr int E = FMT == 0 ? 8 : 32;
   Misc* ms = pp.ms;
   const int lane = tid & 31, warp = tid >> 5;
-  const int C = g.cols / E;
-  int RG, rg, c0, wrg;
-  if (C >= NCT) {
-    RG = 1; rg = 0; c0 = tid; wrg = NCW;
-  } else {
-    const int cpad = (C + 31) & ~31;
-    RG = NCT / cpad; rg = tid / cpad; c0 = tid % cpad; wrg = cpad / 32;
-  }
-  const bool in_group = rg < RG;
-  const int wig = warp - rg * wrg;  // warp index inside its row group
+  const SegInfo si = seg_info(FMT, g.cols);
+  const int nchl = (si.chs + 31) / 32;  // chunks per lane actually used (<= NCHL)
+  const int seg = warp % si.nseg, grp = warp / si.nseg, WG = NCW / si.nseg;
+  const int nrows = rs.r1 - rs.r0;
+  const bool direct = epi.kind == EK_ARGMAX && si.nseg == 1;  // the warp holds whole rows
+  const bool norm = src.gf || src.gb;
 
-  // --- activations: optional RMSNorm over the whole vector, then this thread's chunks
-  float inv = 1.f;
-  if (src.gf || src.gb) {
-    float ss = 0.f;
-    for (int i = tid; i < src.n; i += NCT) {
-      const float v = act_x(src, i);
-      ss = fmaf(v, v, ss);
-    }
-    ss = cons_block_sum(ss, ms, tid);
-    inv = 1.f / sqrtf(ss / (float)src.n + src.eps);
+  // operands of the end-of-phase epilogue, fetched now so that their latency overlaps
+  float pre = 0.f;
+  if (!direct && tid < nrows && epi.kind != EK_ARGMAX) {
+    if (epi.kind == EK_RESIDUAL) pre = __ldcg(epi.y + rs.r0 + tid);
+    else if (epi.kind == EK_STORE && epi.bias) pre = __ldg(epi.bias + rs.r0 + tid);
   }
-  float a[J][E];
-  float S[J];
+
+  // activations of this warp's segment from the shared-memory copy of the input vector; chunks
+  // past the segment read the last valid chunk and are zeroed, so that the row loop needs no
+  // per-lane branches
+  fetch_vector(pp, src.xf ? (const void*)src.xf : (const void*)src.xb,
+               (uint32_t)src.n * (src.xf ? 4u : 2u), tid);
+  float a[NCHL][E];
+  float S[NCHL];
+  float ss = 0.f;
 #pragma unroll
-  for (int j = 0; j < J; ++j) {
-    const int c = c0 + j * NCT;
-    const bool ok = in_group && c < C;
-    S[j] = 0.f;
+  for (int k = 0; k < NCHL; ++k) {
+    const int c = min(lane + 32 * k, si.chs - 1);
+    const int base = seg * si.ks + c * E;
+    const bool ok = lane + 32 * k < si.chs;
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-      float v = 0.f;
-      if (ok) {
-        v = act_x(src, c * E + e);
-        if (src.gf || src.gb) v = v * inv * act_g(src, c * E + e);
+    for (int e = 0; e < E; e += 8) {
+      if (k < nchl) vec8(pp, src.xf != nullptr, base + e, &a[k][e]);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        a[k][e + u] = (ok && k < nchl) ? a[k][e + u] : 0.f;
+        ss = fmaf(a[k][e + u], a[k][e + u], ss);
       }
-      a[j][e] = v;
-      S[j] += v;
-    }
-    if (FMT == 1) {
-#pragma unroll
-      for (int e = 0; e < E; ++e) a[j][e] *= (e & 3) == 0 ? 1.f : (e & 3) == 1 ? 0.0625f : (e & 3) == 2 ? 0.00390625f : 0.000244140625f;
     }
   }
-  const uint32_t scale_off = (uint32_t)(g.cols / 2);
-
-  int buf = 0;
-  for (int s0 = rs.r0; s0 < rs.r1; s0 += rs.nr) {
-    const int nrs = min(rs.nr, rs.r1 - s0);
-    const uint32_t st = cons_acquire(pp);
-    if (in_group) {
-      const int nmine = nrs > rg ? (nrs - rg + RG - 1) / RG : 0;
-      for (int b = 0; b < nmine; b += 8) {
-        float part[8];
+  if (tr_ready && tid == 0) tr_ready[TR_ACT - TR_READY] = globaltimer() + (unsigned long long)(ss * 0.f);
+  if (norm) {
+    float tot = warp_sum(ss);
+    if (si.nseg > 1) {
+      if (grp == 0 && lane == 0) ms->wred[seg] = tot;
+      named_sync(BAR_CONS, NCT);
+      tot = 0.f;
+      for (int s2 = 0; s2 < si.nseg; ++s2) tot += ms->wred[s2];
+    }
+    const float inv = 1.f / sqrtf(tot / (float)src.n + src.eps);
+    // the gain vector is the phase's first ring stage (fp32, or bf16 for the final norm)
+    const uint32_t gs = cons_acquire(pp);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          part[q] = 0.f;
-          if (b + q < nmine) {
-            const uint32_t rowp = st + (uint32_t)(rg + RG * (b + q)) * g.rb;
-            float acc = 0.f;
+    for (int k = 0; k < NCHL; ++k) {
+      if (k < nchl) {
+        const int c = min(lane + 32 * k, si.chs - 1);
+        const int base = seg * si.ks + c * E;
 #pragma unroll
-            for (int j = 0; j < J; ++j) {
-              const int c = c0 + j * NCT;
-              if ((J == 1 || c < C) && c < C) {
-                const uint4 w = lds128(rowp + (uint32_t)c * 16u);
-                if (FMT == 0) {
-                  acc = dot8_bf16(w, a[j], acc);
-                } else {
-                  const float dq = dot32_int4(w, a[j]);
-                  const uint16_t sb = lds16(rowp + scale_off + 2u * (uint32_t)((c * 32) / g.group));
-                  const float sc = g.scale_bf16 ? bf16_to_f(sb) : __half2float(__ushort_as_half(sb));
-                  acc = fmaf(sc, dq - 8.f * S[j], acc);
-                }
-              }
-            }
-            part[q] = acc;
+        for (int e = 0; e < E; e += 8) {
+          float gv[8];
+          if (src.gf) {
+            const uint4 g0 = lds128(gs + (uint32_t)(base + e) * 4u);
+            const uint4 g1 = lds128(gs + (uint32_t)(base + e) * 4u + 16u);
+            gv[0] = __uint_as_float(g0.x); gv[1] = __uint_as_float(g0.y);
+            gv[2] = __uint_as_float(g0.z); gv[3] = __uint_as_float(g0.w);
+            gv[4] = __uint_as_float(g1.x); gv[5] = __uint_as_float(g1.y);
+            gv[6] = __uint_as_float(g1.z); gv[7] = __uint_as_float(g1.w);
+          } else {
+            const uint4 gb = lds128(gs + (uint32_t)(base + e) * 2u);
+            gv[0] = bf16_lo(gb.x); gv[1] = bf16_hi(gb.x); gv[2] = bf16_lo(gb.y); gv[3] = bf16_hi(gb.y);
+            gv[4] = bf16_lo(gb.z); gv[5] = bf16_hi(gb.z); gv[6] = bf16_lo(gb.w); gv[7] = bf16_hi(gb.w);
           }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) a[k][e + u] = a[k][e + u] * inv * gv[u];
         }
-        const float v = transpose_reduce8(part, lane);
-        const int q8 = transpose_row8(lane);
-        if ((lane & 3) == 0 && b + q8 < nmine) ms->red[buf][rg + RG * (b + q8)][wig] = v;
       }
     }
     cons_release(pp, lane);
-    named_sync(BAR_CONS, NCT);
-    if (epi.kind == EK_SWIGLU) {
-      if (tid < nrs / 2) {
-        float gt = 0.f, up = 0.f;
-        for (int w = 0; w < wrg; ++w) gt += ms->red[buf][2 * tid][w];
-        for (int w = 0; w < wrg; ++w) up += ms->red[buf][2 * tid + 1][w];
-        epi.y[s0 / 2 + tid] = gt / (1.f + expf(-gt)) * up;
-      }
-    } else if (tid < nrs) {
-      float v = 0.f;
-      for (int w = 0; w < wrg; ++w) v += ms->red[buf][tid][w];
-      const int r = s0 + tid;
-      if (epi.kind == EK_STORE) {
-        epi.y[r] = epi.bias ? v + epi.bias[r] : v;
-      } else if (epi.kind == EK_RESIDUAL) {
-        epi.y[r] += v;
-      } else {  // EK_ARGMAX
+  }
+  if (FMT == 1) {
+#pragma unroll
+    for (int k = 0; k < NCHL; ++k) {
+      float t = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) t += a[k][e];
+      S[k] = t;
+#pragma unroll
+      for (int e = 0; e < E; ++e)
+        a[k][e] *= (e & 3) == 0 ? 1.f : (e & 3) == 1 ? 0.0625f : (e & 3) == 2 ? 0.00390625f : 0.000244140625f;
+    }
+  }
+  if (tr_ready && tid == 0) *tr_ready = globaltimer();
+
+  const uint32_t seg_off = FMT == 0 ? (uint32_t)(seg * si.ks * 2) : (uint32_t)(seg * si.ks / 2);
+  const uint32_t scale_off = (uint32_t)(g.cols / 2);
+  const int lane_c = lane;  // chunk k of this lane is lane + 32 k, clamped to the segment
+
+  // The warp walks its rows stage by stage (rows grp, grp + WG, ... of each stage). Lane partials
+  // of the last eight rows ride in a shift window; a full window is finished by one transposed
+  // reduction (9 shuffles for 8 rows). A stage is released as soon as the warp's last row in it
+  // has been read.
+  float w0 = 0.f, w1 = 0.f, w2 = 0.f, w3 = 0.f, w4 = 0.f, w5 = 0.f, w6 = 0.f, w7 = 0.f;
+  int r0 = -1, r1 = -1, r2 = -1, r3 = -1, r4 = -1, r5 = -1, r6 = -1, r7 = -1;
+  int filled = 0;
+  auto flush = [&]() {
+    const float part[8] = {w0, w1, w2, w3, w4, w5, w6, w7};
+    const int rid[8] = {r0, r1, r2, r3, r4, r5, r6, r7};
+    const float v = transpose_reduce8(part, lane);
+    const int q8 = transpose_row8(lane);
+    int rl = -1;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) rl = q == q8 ? rid[q] : rl;
+    if ((lane & 3) == 0 && rl >= 0) {
+      if (direct) {
+        const int r = rs.r0 + rl;
         if (epi.y) epi.y[r] = v;
         best_update(best, v, r);
+      } else {
+        ms->rowv[rl * si.nseg + seg] = v;
       }
     }
-    buf ^= 1;
+    w0 = w1 = w2 = w3 = w4 = w5 = w6 = w7 = 0.f;
+    r0 = r1 = r2 = r3 = r4 = r5 = r6 = r7 = -1;
+    filled = 0;
+  };
+  for (int s0 = rs.r0; s0 < rs.r1; s0 += rs.nr) {
+    const int nrs = min(rs.nr, rs.r1 - s0);
+    const uint32_t st = cons_acquire(pp);
+#pragma unroll 1
+    for (int i = grp; i < nrs; i += WG) {
+      const uint32_t rowp = st + (uint32_t)i * g.rb;
+      float2 acc = make_float2(0.f, 0.f), acc2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < NCHL; ++k) {
+        if (k < nchl) {
+          const int c = min(lane_c + 32 * k, si.chs - 1);
+          const uint4 w = lds128(rowp + seg_off + (uint32_t)c * 16u);
+          if (FMT == 0) {
+            if (k & 1) acc2 = dot8_bf16(w, a[k], acc2);
+            else acc = dot8_bf16(w, a[k], acc);
+          } else {
+            const float dq = dot32_int4(w, a[k]);
+            const uint16_t sb = lds16(rowp + scale_off + 2u * (uint32_t)((seg * si.ks + c * 32) / g.group));
+            const float sc = g.scale_bf16 ? bf16_to_f(sb) : __half2float(__ushort_as_half(sb));
+            acc.x = fmaf(sc, dq - 8.f * S[k], acc.x);
+          }
+        }
+      }
+      // shift the window: the newest row enters at w0
+      w7 = w6; w6 = w5; w5 = w4; w4 = w3; w3 = w2; w2 = w1; w1 = w0;
+      r7 = r6; r6 = r5; r5 = r4; r4 = r3; r3 = r2; r2 = r1; r1 = r0;
+      w0 = (acc.x + acc.y) + (acc2.x + acc2.y);
+      r0 = (s0 - rs.r0) + i;
+      if (++filled == 8) flush();
+    }
+    cons_release(pp, lane);
+  }
+  if (filled) flush();
+  if (direct) return;
+  named_sync(BAR_CONS, NCT);
+  if (epi.kind == EK_SWIGLU) {
+    for (int p = tid; p < nrows / 2; p += NCT) {
+      float gt = 0.f, up = 0.f;
+      for (int s2 = 0; s2 < si.nseg; ++s2) gt += ms->rowv[(2 * p) * si.nseg + s2];
+      for (int s2 = 0; s2 < si.nseg; ++s2) up += ms->rowv[(2 * p + 1) * si.nseg + s2];
+      epi.y[rs.r0 / 2 + p] = gt / (1.f + expf(-gt)) * up;
+    }
+  } else {
+    for (int t = tid; t < nrows; t += NCT) {
+      float v = 0.f;
+      for (int s2 = 0; s2 < si.nseg; ++s2) v += ms->rowv[t * si.nseg + s2];
+      const int r = rs.r0 + t;
+      if (epi.kind == EK_ARGMAX) {
+        if (epi.y) epi.y[r] = v;
+        best_update(best, v, r);
+        continue;
+      }
+      float base = pre;
+      if (t >= NCT) base = epi.kind == EK_RESIDUAL ? __ldcg(epi.y + r) : (epi.bias ? epi.bias[r] : 0.f);
+      epi.y[r] = (epi.kind == EK_RESIDUAL || epi.bias) ? base + v : v;
+    }
   }
 }
 
-// Runtime dispatch to the template instance for (format, chunks per thread).
-__device__ __noinline__ void gemv_consume_any(Pipe& pp, const GemvDesc& g, const RowSplit& rs,
-                                              const ActSrc& src, const Epi& epi, Best& best,
-                                              int tid) {
-  if (g.fmt == 1) {
-    gemv_consume<1, 1>(pp, g, rs, src, epi, best, tid);
-    return;
-  }
-  const int C = g.cols / 8;
-  const int J = (C + NCT - 1) / NCT;
-  switch (J) {
-    case 1: gemv_consume<0, 1>(pp, g, rs, src, epi, best, tid); break;
-    case 2: gemv_consume<0, 2>(pp, g, rs, src, epi, best, tid); break;
-    case 3: gemv_consume<0, 3>(pp, g, rs, src, epi, best, tid); break;
-    case 4: gemv_consume<0, 4>(pp, g, rs, src, epi, best, tid); break;
-    default: gemv_consume<0, 5>(pp, g, rs, src, epi, best, tid); break;
-  }
+// Dispatch to the instance of the weight format (the chunk count per lane is a runtime bound).
+__device__ __forceinline__ void gemv_consume_any(Pipe& pp, const GemvDesc& g, const RowSplit& rs,
+                                                 const ActSrc& src, const Epi& epi, Best& best,
+                                                 int tid, unsigned long long* tr_ready) {
+  if (g.fmt == 1) gemv_rows<1, 2>(pp, g, rs, src, epi, best, tid, tr_ready);
+  else gemv_rows<0, 8>(pp, g, rs, src, epi, best, tid, tr_ready);
 }
 
 __device__ __forceinline__ void produce_rows(Pipe& pp, const GemvDesc& g, const RowSplit& rs,
-                                             uint64_t pol, bool& dead) {
+                                             uint64_t pol, bool& dead, const void* gain = nullptr,
+                                             uint32_t gain_bytes = 0) {
+  if (gain_bytes) prod_push(pp, gain, gain_bytes, pol, dead);
   for (int s0 = rs.r0; s0 < rs.r1; s0 += rs.nr) {
     const int nrs = min(rs.nr, rs.r1 - s0);
     prod_push(pp, g.w + (size_t)s0 * g.rb, (uint32_t)(nrs * g.rb), pol, dead);
@@ -510,13 +623,11 @@ __device__ void argmax_publish(const Best& mine, float* slot_v, int* slot_i, int
     slot_v[cta] = mine.v;
     slot_i[cta] = mine.i;
     slot_bad[cta] = mine.bad;
-    __threadfence();
-    const unsigned old = atomicAdd(ticket, 1u);
+    const unsigned old = atom_add_acq_rel(ticket, 1u);
     ms->flag = (old == (unsigned)nslots - 1);
   }
   named_sync(BAR_CONS, NCT);
   if (ms->flag && tid < 32) {
-    __threadfence();
     Best b{-CUDART_INF_F, 0x7FFFFFFF, 0};
     for (int s = tid; s < nslots; s += 32) {
       const float v = __ldcg(slot_v + s);
@@ -594,7 +705,9 @@ __device__ __forceinline__ void produce_attn_unit(Pipe& pp, const AttnArgs& A, i
   prod_push(pp, A.vc + base, (uint32_t)(nk * A.d * 2), pol, dead);
 }
 
-// Merge of one KV head's chunk partials for its query heads (the log-sum-exp combine).
+// Merge of one KV head's chunk partials for its query heads (the log-sum-exp combine). Warp g finds
+// head g's maximum and weights (lanes over chunks), then each output element sums its chunks'
+// unnormalised outputs in a fixed order, eight loads in flight at a time.
 __device__ void attn_merge(const AttnArgs& A, Misc* ms, int tid, int j, int nch) {
   const int G = A.nq / A.nkv, d = A.d;
   const int warp = tid >> 5, lane = tid & 31;
@@ -606,8 +719,7 @@ __device__ void attn_merge(const AttnArgs& A, Misc* ms, int tid, int j, int nch)
     float den = 0.f;
     for (int c = lane; c < nch; c += 32) {
       const float mc = __ldcg(A.part_m + (size_t)h * A.nch_cap + c);
-      float w = 0.f;
-      if (mc != -CUDART_INF_F) w = expf(mc - M);  // an empty chunk weighs exactly 0
+      const float w = mc == -CUDART_INF_F ? 0.f : expf(mc - M);  // an empty chunk weighs exactly 0
       ms->sc[warp * T_MAX + c] = w;
       den = fmaf(w, __ldcg(A.part_l + (size_t)h * A.nch_cap + c), den);
     }
@@ -620,7 +732,15 @@ __device__ void attn_merge(const AttnArgs& A, Misc* ms, int tid, int j, int nch)
     const int h = j * G + g;
     const float* po = A.part_o + (size_t)h * A.nch_cap * d + i;
     float acc = 0.f;
-    for (int c = 0; c < nch; ++c) acc = fmaf(ms->sc[g * T_MAX + c], __ldcg(po + (size_t)c * d), acc);
+    int c = 0;
+    for (; c + 8 <= nch; c += 8) {
+      float o[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) o[u] = __ldcg(po + (size_t)(c + u) * d);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) acc = fmaf(ms->sc[g * T_MAX + c + u], o[u], acc);
+    }
+    for (; c < nch; ++c) acc = fmaf(ms->sc[g * T_MAX + c], __ldcg(po + (size_t)c * d), acc);
     A.out[(size_t)h * d + i] = acc * ms->hl[g];
   }
 }
@@ -751,15 +871,15 @@ __device__ void attn_unit(Pipe& pp, const AttnArgs& A, const AttnSplit& sp, int 
     A.part_m[(size_t)h * A.nch_cap + c] = ms->hm[tid];
     A.part_l[(size_t)h * A.nch_cap + c] = ms->hl[tid];
   }
-  __threadfence();
   named_sync(BAR_CONS, NCT);
   if (tid == 0) {
-    const unsigned old = atomicAdd(A.tickets + j, 1u);
+    // release publishes this CTA's partials (ordered before by the barrier); acquire makes the
+    // other CTAs' partials visible to the merging CTA
+    const unsigned old = atom_add_acq_rel(A.tickets + j, 1u);
     ms->flag = (old == (unsigned)sp.nch - 1);
   }
   named_sync(BAR_CONS, NCT);
   if (ms->flag) {
-    __threadfence();
     attn_merge(A, ms, tid, j, sp.nch);
     if (tid == 0) atomicExch(A.tickets + j, 0u);
   }

@@ -139,8 +139,18 @@ tinfer_status tinfer_get_error(tinfer_ctx* ctx);
  * shared memory per CTA of the persistent kernel), TINFER_Q_RING_STAGES, TINFER_Q_SLOT_BYTES,
  * TINFER_Q_KERNELS_PER_STEP (kernel launches one step makes). Returns -1 for an unknown query. */
 enum { TINFER_Q_GRID = 0, TINFER_Q_SMEM = 1, TINFER_Q_RING_STAGES = 2, TINFER_Q_SLOT_BYTES = 3,
-       TINFER_Q_KERNELS_PER_STEP = 4 };
+       TINFER_Q_KERNELS_PER_STEP = 4, TINFER_Q_TRACE_BYTES = 5 };
 long long tinfer_query(const tinfer_ctx* ctx, int what);
+
+/* Per-worker timeline of the persistent kernel ("Decoding in tiles", section 5, Figure 9: each
+ * worker's time split into streaming, waiting and small work). When trace_dev is not NULL (device
+ * memory of TINFER_Q_TRACE_BYTES bytes, caller-owned), every following megakernel step writes, for
+ * every CTA c and phase k (k = 5*layer + {0 QKV, 1 attention, 2 O, 3 gate/up, 4 down}, the LM head
+ * last), six uint64 %globaltimer nanosecond stamps at [(c * phases + k) * 6 + f]: f = 0 phase start
+ * (after the previous grid barrier), 1 activations normalised and ready, 2 phase end, 3 producer
+ * starts issuing the phase's copies, 4 producer has issued them, 5 input activations arrived (GEMV
+ * phases). NULL turns tracing off. */
+tinfer_status tinfer_set_trace(tinfer_ctx* ctx, void* trace_dev);
 
 /* Test hooks: timeout of every device-side wait in nanoseconds (default 200 ms), and a fault
  * injected on the host side of the contract: CTA `cta` skips its arrival at grid barrier number

@@ -54,6 +54,7 @@ def test_invalid_and_unsupported_configs_are_rejected():
         (dict(weight_format="int4", group_size=48), T.TINFER_ERR_UNSUPPORTED),
         (dict(weight_format="int4", group_size=64), T.TINFER_ERR_UNSUPPORTED),  # ffn 688 not /64
         (dict(max_ctx=10 ** 6), T.TINFER_ERR_UNSUPPORTED),
+        (dict(n_layers=65), T.TINFER_ERR_UNSUPPORTED),
     ]
     for over, want in cases:
         c = dict(base)

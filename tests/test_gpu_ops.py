@@ -89,8 +89,9 @@ def test_gemv_bf16_matches_oracle(rows, cols):
     np.testing.assert_allclose(y, ref, rtol=1e-4, atol=2e-5 * np.sqrt(cols / 256))
 
 
-def test_gemv_rmsnorm_prologue_matches_oracle():
-    rows, cols = 515, 2048
+@pytest.mark.parametrize("cols", [2048, 2560, 8192])  # one, two and four row segments
+def test_gemv_rmsnorm_prologue_matches_oracle(cols):
+    rows = 515
     rng = np.random.default_rng(3)
     W = synth.normal_bf16("gemvnorm", (rows, cols), 0.0, 0.02)
     x = (3 * rng.standard_normal(cols)).astype(np.float32)
@@ -130,6 +131,13 @@ def test_gemv_argmax_ties_lowest_index_and_nonfinite():
     assert rc == 0 and am == 17 and y[17] == y[4321]
     ref = ORC.gemv_bf16(W, x.astype(np.float64))
     assert ORC.argmax(ref)[0] == 17
+    # the same with rows wider than one segment (the LM head of a 2560-wide model)
+    W3 = synth.normal_bf16("argmax3", (3000, 2560), 0.0, 0.02)
+    W3[2999] = W3[1500] = synth.normal_bf16("hot3", (2560,), 0.25, 0.0)
+    rc, y3, am3 = gemv(T.TINFER_BF16, 0, 0, pack(T.TINFER_BF16, 0, 0, W3), 3000, 2560,
+                       np.ones(2560, np.float32), epi=T.TINFER_EPI_ARGMAX)
+    assert rc == 0 and am3 == 1500
+    np.testing.assert_allclose(y3, ORC.gemv_bf16(W3, np.ones(2560)), rtol=1e-4, atol=1e-4)
     W2 = W.copy()
     W2[999, 5] = 0x7FC0  # NaN
     p2 = pack(T.TINFER_BF16, 0, 0, W2)
