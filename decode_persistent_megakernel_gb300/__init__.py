@@ -313,7 +313,7 @@ class Engine:
         _check(rc, "tinfer_decode_step_dev")
 
     def trace_step(self, token: int, pos: int):
-        """Runs one traced megakernel step; returns int64 stamps [grid][phases][6] (ns, relative to
+        """Runs one traced megakernel step; returns int64 stamps [grid][phases][8] (ns, relative to
         the earliest stamp)."""
         import numpy as np
         import torch
@@ -323,7 +323,7 @@ class Engine:
         self.step(token, pos)
         torch.cuda.synchronize()
         _check(tinfer_set_trace(self.ctx, None), "tinfer_set_trace")
-        t = buf.cpu().numpy().reshape(self.query(TINFER_Q_GRID), -1, 6)
+        t = buf.cpu().numpy().reshape(self.query(TINFER_Q_GRID), -1, 8)
         return t - t[t > 0].min()
 
     def error(self) -> int:

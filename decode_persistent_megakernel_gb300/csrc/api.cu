@@ -128,6 +128,13 @@ const char* tinfer_status_string(tinfer_status s) {
   return "unknown status";
 }
 
+// The bf16 GEMV instance of the step kernels for a model: bf16 models stream every matrix in bf16,
+// int4 models only the LM head.
+static int model_nchl(const tinfer_config* c) {
+  const int cols[4] = {c->hidden, c->n_heads * c->head_dim, c->ffn, c->hidden};
+  return c->weight_format == TINFER_BF16 ? nchl_instance(cols, 4) : nchl_instance(cols + 3, 1);
+}
+
 tinfer_status tinfer_check_config(const tinfer_config* c) {
   if (!c) return TINFER_ERR_INVALID_ARG;
   if (c->n_layers <= 0 || c->hidden <= 0 || c->n_heads <= 0 || c->n_kv_heads <= 0 ||
@@ -150,6 +157,7 @@ tinfer_status tinfer_check_config(const tinfer_config* c) {
       c->scale_dtype != TINFER_SCALE_BF16)
     return TINFER_ERR_INVALID_ARG;
   if (c->hidden % 8 != 0 || !seg_ok(TINFER_BF16, c->hidden)) return TINFER_ERR_UNSUPPORTED;  // LM head
+  if (model_nchl(c) == 0) return TINFER_ERR_UNSUPPORTED;
   if ((size_t)c->hidden * 4 > (size_t)slot_bytes_for(c)) return TINFER_ERR_UNSUPPORTED;  // gain stage
   const int slot = slot_bytes_for(c);
   int tmax = slot / (2 * c->head_dim);
@@ -312,6 +320,7 @@ tinfer_status tinfer_create(const tinfer_config* c, const tinfer_weights* w, voi
   x->slot = slot_bytes_for(c);
   x->xs_bytes = xs_bytes_for(c);
   const size_t misc = smem_for(0, 0, x->xs_bytes);
+  smem_optin -= 256;  // the persistent kernel's static shared memory
   x->stages_mega = (int)((smem_optin - misc) / x->slot);
   if (x->stages_mega > 8) x->stages_mega = 8;
   while (x->stages_mega > 2 && smem_for(x->stages_mega, x->slot, x->xs_bytes) > (size_t)smem_optin) --x->stages_mega;
@@ -323,10 +332,11 @@ tinfer_status tinfer_create(const tinfer_config* c, const tinfer_weights* w, voi
   if (x->stages_mega < 2 || x->stages_phase < 2) return fail(TINFER_ERR_UNSUPPORTED);
   x->smem_mega = smem_for(x->stages_mega, x->slot, x->xs_bytes);
   x->smem_phase = smem_for(x->stages_phase, x->slot, x->xs_bytes);
-  if ((st = cu(set_smem_mega(x->smem_mega))) != TINFER_OK) return fail(st);
-  if ((st = cu(set_smem_phase(x->smem_phase))) != TINFER_OK) return fail(st);
+  const int nchl = model_nchl(c);
+  if ((st = cu(set_smem_mega(x->smem_mega, c->weight_format, nchl))) != TINFER_OK) return fail(st);
+  if ((st = cu(set_smem_phase(x->smem_phase, c->weight_format, nchl))) != TINFER_OK) return fail(st);
   int occ = 0;
-  if ((st = cu(megakernel_occupancy(&occ, x->smem_mega, c->weight_format))) != TINFER_OK) return fail(st);
+  if ((st = cu(megakernel_occupancy(&occ, x->smem_mega, c->weight_format, nchl))) != TINFER_OK) return fail(st);
   if (occ < 1) return fail(TINFER_ERR_UNSUPPORTED);
   const int grid = x->num_sms;  // one persistent CTA per SM (co-residency: cooperative launch)
   {
@@ -394,6 +404,7 @@ tinfer_status tinfer_create(const tinfer_config* c, const tinfer_weights* w, voi
   m.rb_f = (int)packed_row_bytes(m.fmt, F, m.group);
   m.rb_lm = H * 2;
   m.qkv_rows = qkv_rows;
+  m.nchl = nchl;
   for (int l = 0; l < c->n_layers; ++l) p.layers[l] = ld[l];
   p.embed = (const uint16_t*)w->embed;
   p.lm_head = (const uint16_t*)w->lm_head;
@@ -412,6 +423,15 @@ tinfer_status tinfer_create(const tinfer_config* c, const tinfer_weights* w, voi
   p.grid = grid;
   p.slot_bytes = x->slot;
   p.inflight = 2;
+  p.l2_lookahead = 512 * 1024;
+  p.l2_pace_ns_per_kb = 24;
+  {
+    // tuning overrides for experiments: TINFER_L2_LOOKAHEAD (bytes per CTA, 0 = off),
+    // TINFER_L2_PACE (ns per KB), TINFER_INFLIGHT (bulk copies outstanding)
+    if (const char* e = getenv("TINFER_L2_LOOKAHEAD")) p.l2_lookahead = atoi(e);
+    if (const char* e = getenv("TINFER_L2_PACE")) p.l2_pace_ns_per_kb = atoi(e);
+    if (const char* e = getenv("TINFER_INFLIGHT")) p.inflight = atoi(e);
+  }
   p.bar_base = 0;
   p.timeout_ns = DEFAULT_TIMEOUT_NS;
   p.step_dev = (int*)(s + o_step);

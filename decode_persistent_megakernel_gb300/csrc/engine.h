@@ -3,6 +3,12 @@
 #include <cstddef>
 #include <cstdint>
 
+#ifdef __CUDACC__
+#define TINFER_HD __host__ __device__
+#else
+#define TINFER_HD
+#endif
+
 namespace tinfer {
 
 // Thread block: NCW consumer warps that compute, plus one producer warp whose elected lane streams
@@ -12,11 +18,11 @@ constexpr int NCT = NCW * 32;
 constexpr int NTHREADS = NCT + 32;
 // The persistent kernel runs a 4-warp producer group instead of one producer warp, so that the two
 // groups can trade registers (setmaxnreg): the producer group keeps REG_PRODUCER registers per
-// thread, the consumer warps grow to REG_CONSUMER. Launch total: 12 warps x 32 x 168 = 64512 =
-// 8 x 32 x REG_CONSUMER + 4 x 32 x REG_PRODUCER.
+// thread (its copy cursor and the L2 lookahead cursor), the consumer warps grow to REG_CONSUMER.
+// Launch total: 12 warps x 32 x 168 = 64512 = 8 x 32 x REG_CONSUMER + 4 x 32 x REG_PRODUCER.
 constexpr int NTHREADS_MEGA = NCT + 128;
-constexpr int REG_CONSUMER = 232;
-constexpr int REG_PRODUCER = 40;
+constexpr int REG_CONSUMER = 200;
+constexpr int REG_PRODUCER = 104;
 static_assert(NCW * 32 * REG_CONSUMER + 4 * 32 * REG_PRODUCER <= (NTHREADS_MEGA / 32) * 32 * 168,
               "register split exceeds the launch allocation");
 constexpr int NR_MAX = 32;    // rows of one matrix held by one ring stage, at most
@@ -35,7 +41,7 @@ enum : int {
   EW_BADTOKEN = 4,
 };
 
-struct LayerDev {
+struct __align__(8) LayerDev {
   const uint8_t* qkv;   // [(nq + 2 nkv) d] packed rows of hidden inputs
   const uint8_t* o;     // [hidden] packed rows of nq*d inputs
   const uint8_t* gu;    // [2 ffn] packed rows (gate, up interleaved) of hidden inputs
@@ -54,10 +60,12 @@ struct Dims {
   int rb_h, rb_qd, rb_f;  // packed row bytes for hidden, nq*d and ffn inputs
   int rb_lm;              // bf16 LM head row bytes (2 * hidden)
   int qkv_rows;           // (nq + 2 nkv) * d
+  int nchl;               // bf16 GEMV instance of the step kernels: 16-byte chunks per lane (4, 6, 8)
 };
 
-// Everything one step needs; passed by value to every kernel.
-struct StepParams {
+// Everything one step needs; passed by value to every kernel (16-byte multiple: copied to shared
+// memory in 16-byte words).
+struct __align__(16) StepParams {
   Dims m;
   LayerDev layers[MAX_LAYERS];  // read through the constant cache
   const uint16_t* embed;
@@ -86,6 +94,8 @@ struct StepParams {
   int ring_stages;
   int slot_bytes;
   int inflight;            // bulk copies the producer keeps outstanding at most
+  int l2_lookahead;        // persistent kernel: bytes per CTA prefetched into L2 ahead of the ring
+  int l2_pace_ns_per_kb;   // spacing of those prefetches (about the per-SM share of HBM bandwidth)
   long long timeout_ns;
   // per step
   int token;               // used when token_dev is null
@@ -107,8 +117,10 @@ enum TraceField : int {
   TR_END = 2,        // consumers done with the phase (before the grid barrier)
   TR_PROD_BEGIN = 3, // producer starts issuing the phase's copies
   TR_PROD_END = 4,   // producer has issued the phase's last copy
-  TR_ACT = 5,        // the phase's input activations have arrived (before the norm)
-  TRACE_FIELDS = 6
+  TR_ACT = 5,        // the phase's input activations are in registers (before the norm)
+  TR_ENTRY = 6,      // the GEMV code of the phase starts (after the phase set-up)
+  TR_FETCHED = 7,    // the input vector is in shared memory
+  TRACE_FIELDS = 8
 };
 
 // Op-level GEMV description (the single-operation entry point uses the same device code).
@@ -127,11 +139,6 @@ struct GemvOp {
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-#ifdef __CUDACC__
-#define TINFER_HD __host__ __device__
-#else
-#define TINFER_HD
-#endif
 
 constexpr int SEG_MAX_INPUTS = 2048;  // inputs of one row segment (activations held per lane: 64)
 constexpr int ROWV_MAX = 1024;        // row results of one phase kept in shared memory per CTA
@@ -165,6 +172,18 @@ TINFER_HD inline int stage_rows(int fmt, int cols, int rb, int slot, int quantum
   int nr = fit - fit % step;
   if (nr == 0) nr = fit - fit % quantum;
   return nr;
+}
+
+// The bf16 GEMV instance (chunks per lane, 4, 6 or 8) that covers rows of every given width; 0 when
+// some width does not fit the register budget.
+inline int nchl_instance(const int* cols, int n) {
+  int need = 1;
+  for (int i = 0; i < n; ++i) {
+    if (!seg_ok(0, cols[i])) return 0;
+    const int c = (seg_info(0, cols[i]).chs + 31) / 32;
+    if (c > need) need = c;
+  }
+  return need <= 4 ? 4 : need <= 6 ? 6 : 8;
 }
 
 // Packed row bytes: bf16 rows are 2*cols (cols % 8 == 0); int4 rows are cols/2 nibble bytes plus

@@ -50,12 +50,12 @@ cudaError_t launch_begin(int* step_dev, int token, const int* token_dev, int pos
 const void* begin_kernel_fn();
 cudaError_t launch_op_gemv(const OpGemvParams& q, int grid, size_t smem, cudaStream_t st);
 cudaError_t launch_op_attention(const OpAttnParams& q, int grid, size_t smem, cudaStream_t st);
-cudaError_t set_smem_mega(size_t bytes);
-cudaError_t set_smem_phase(size_t bytes);
+cudaError_t set_smem_mega(size_t bytes, int fmt, int nchl);
+cudaError_t set_smem_phase(size_t bytes, int fmt, int nchl);
 cudaError_t set_smem_op_gemv(size_t bytes);
 cudaError_t set_smem_op_attention(size_t bytes);
-cudaError_t megakernel_occupancy(int* blocks_per_sm, size_t smem, int fmt);
-cudaError_t phase_occupancy(int* blocks_per_sm, size_t smem, int fmt);
+cudaError_t megakernel_occupancy(int* blocks_per_sm, size_t smem, int fmt, int nchl);
+cudaError_t phase_occupancy(int* blocks_per_sm, size_t smem, int fmt, int nchl);
 size_t smem_for(int stages, int slot, int xs_bytes);
 
 cudaError_t launch_pack_rows(uint8_t* dst, int dst_rb, int dst_step, int dst_first, int rows,

@@ -1,0 +1,484 @@
+// megakernel.cuh -- device side of the decode step: the step schedule, the persistent producer,
+// the consumer phases, the persistent kernel and the per-phase kernel. Included by the translation
+// units that instantiate the kernels (one per weight format, so that they compile in parallel).
+//
+// The kernels are templates over the weight format, the number of 16-byte chunks a lane holds in
+// the bf16 GEMV (NCHL) and, for the persistent kernel, whether it records a timeline. One bf16 GEMV
+// width per kernel keeps the register allocation of the persistent kernel free of spills: the host
+// picks the instance that covers every bf16 matrix of the model.
+#pragma once
+#include <cuda_runtime.h>
+
+#include "engine.h"
+#include "kernels.h"
+#include "step.cuh"
+
+namespace tinfer {
+
+// ------------------------------------------------------------------------------ step schedule
+
+__device__ __forceinline__ void phase_of(int k, int L, int& phase, int& layer) {
+  if (k >= L * PHASES_PER_LAYER) { phase = PH_LM; layer = 0; return; }
+  layer = k / PHASES_PER_LAYER;
+  const int r = k - layer * PHASES_PER_LAYER;
+  phase = r == 0 ? PH_QKV : r == 1 ? PH_ATTN : r == 2 ? PH_O : r == 3 ? PH_GU : PH_DOWN;
+}
+
+__device__ __forceinline__ GemvDesc phase_gemv(const StepParams& p, int phase, int layer) {
+  const Dims& m = p.m;
+  GemvDesc g;
+  g.fmt = m.fmt;
+  g.group = m.group;
+  g.scale_bf16 = m.scale_bf16;
+  g.quantum = 1;
+  const LayerDev& L = p.layers[layer];
+  switch (phase) {
+    case PH_QKV: g.w = L.qkv; g.rows = m.qkv_rows; g.cols = m.H; g.rb = m.rb_h; break;
+    case PH_O: g.w = L.o; g.rows = m.H; g.cols = m.nq * m.d; g.rb = m.rb_qd; break;
+    case PH_GU: g.w = L.gu; g.rows = 2 * m.F; g.cols = m.H; g.rb = m.rb_h; g.quantum = 2; break;
+    case PH_DOWN: g.w = L.down; g.rows = m.H; g.cols = m.F; g.rb = m.rb_f; break;
+    default:
+      g.w = reinterpret_cast<const uint8_t*>(p.lm_head);
+      g.rows = m.V; g.cols = m.H; g.rb = m.rb_lm; g.fmt = 0;
+      break;
+  }
+  return g;
+}
+
+__device__ __forceinline__ AttnArgs step_attn_args(const StepParams& p, int layer, int pos) {
+  const Dims& m = p.m;
+  AttnArgs A;
+  A.qkv = p.qkv;
+  const size_t lay = (size_t)layer * m.nkv * m.max_ctx * m.d;
+  A.kc = p.kcache + lay;
+  A.vc = p.vcache + lay;
+  A.rope = p.rope;
+  A.part_m = p.part_m;
+  A.part_l = p.part_l;
+  A.part_o = p.part_o;
+  A.nch_cap = p.nch_cap;
+  A.tickets = p.tickets;
+  A.out = p.attn;
+  A.nq = m.nq; A.nkv = m.nkv; A.d = m.d; A.max_ctx = m.max_ctx; A.pos = pos;
+  return A;
+}
+
+__device__ __forceinline__ void produce_phase(const StepParams& p, Pipe& pp, int phase, int layer, int pos,
+                              uint64_t pol_w, uint64_t pol_kv, bool& dead) {
+  if (phase == PH_ATTN) {
+    const AttnArgs A = step_attn_args(p, layer, pos);
+    const AttnSplit sp = attn_split(pos, A.nkv, A.d, p.grid, p.slot_bytes, p.n_chunks_override);
+    const int units = A.nkv * sp.nch;
+    for (int u = blockIdx.x; u < units; u += p.grid)
+      produce_attn_unit(pp, A, u / sp.nch, u % sp.nch, sp, pol_kv, dead);
+    return;
+  }
+  const GemvDesc g = phase_gemv(p, phase, layer);
+  const void* gain = nullptr;
+  uint32_t gain_bytes = 0;
+  if (phase == PH_QKV) { gain = p.layers[layer].g1; gain_bytes = p.m.H * 4; }
+  else if (phase == PH_GU) { gain = p.layers[layer].g2; gain_bytes = p.m.H * 4; }
+  else if (phase == PH_LM) { gain = p.final_norm; gain_bytes = p.m.H * 2; }
+  produce_rows(pp, g, row_split(g, blockIdx.x, p.grid, p.slot_bytes), pol_w, dead, gain, gain_bytes);
+}
+
+// Timeline slot of (this CTA, phase k, field); null when the launch records no timeline. The
+// persistent kernel passes a compile-time null in its untraced instance, so that the stamps cost
+// nothing there.
+__device__ __forceinline__ unsigned long long* trace_at(unsigned long long* trace, const StepParams& p,
+                                                        int k, int field) {
+  if (!trace) return nullptr;
+  const int nph = p.m.L * PHASES_PER_LAYER + 1;
+  return trace + ((size_t)blockIdx.x * nph + k) * TRACE_FIELDS + field;
+}
+
+// The persistent producer's view of the step: one pass over this CTA's copy schedule, stage by
+// stage, in the order the consumers take them (per GEMV phase the gain vector if the phase
+// normalises, then its rows; per attention unit the cached K chunk, then the V chunk).
+struct StageCursor {
+  int k, j;                        // phase index, stage within the phase (-1: gain stage)
+  int attn;                        // the phase is attention
+  const uint8_t* w;                // GEMV: matrix, row bytes, this CTA's rows, rows per stage
+  int rb, r0, r1, nr;
+  const void* gain;
+  int gain_bytes;
+  const uint16_t* kc;              // attention: this layer's K and V caches
+  const uint16_t* vc;
+  int u, units, nch, cl, sub;      // unit cursor, split, K/V half of the unit
+};
+
+static __device__ void cursor_enter(const StepParams& p, StageCursor& c, int pos) {
+  const int nph = p.m.L * PHASES_PER_LAYER + 1;
+  if (c.k >= nph) return;
+  int phase, layer;
+  phase_of(c.k, p.m.L, phase, layer);
+  if (phase == PH_ATTN) {
+    const AttnSplit sp = attn_split(pos, p.m.nkv, p.m.d, p.grid, p.slot_bytes, p.n_chunks_override);
+    const size_t lay = (size_t)layer * p.m.nkv * p.m.max_ctx * p.m.d;
+    c.attn = 1; c.kc = p.kcache + lay; c.vc = p.vcache + lay;
+    c.nch = sp.nch; c.cl = sp.cl; c.units = p.m.nkv * sp.nch; c.u = blockIdx.x; c.sub = 0;
+    return;
+  }
+  const GemvDesc g = phase_gemv(p, phase, layer);
+  const RowSplit rs = row_split(g, blockIdx.x, p.grid, p.slot_bytes);
+  c.attn = 0; c.w = g.w; c.rb = g.rb; c.r0 = rs.r0; c.r1 = rs.r1; c.nr = rs.nr;
+  c.gain = nullptr; c.gain_bytes = 0;
+  if (phase == PH_QKV) { c.gain = p.layers[layer].g1; c.gain_bytes = p.m.H * 4; }
+  else if (phase == PH_GU) { c.gain = p.layers[layer].g2; c.gain_bytes = p.m.H * 4; }
+  else if (phase == PH_LM) { c.gain = p.final_norm; c.gain_bytes = p.m.H * 2; }
+  c.j = c.gain ? -1 : 0;
+}
+
+static __device__ bool cursor_next(const StepParams& p, StageCursor& c, int pos, const void*& src,
+                            uint32_t& bytes) {
+  const int nph = p.m.L * PHASES_PER_LAYER + 1;
+  while (c.k < nph) {
+    if (!c.attn) {
+      if (c.j < 0) { src = c.gain; bytes = (uint32_t)c.gain_bytes; c.j = 0; return true; }
+      const int s0 = c.r0 + c.j * c.nr;
+      if (s0 < c.r1) {
+        src = c.w + (size_t)s0 * c.rb;
+        bytes = (uint32_t)(min(c.nr, c.r1 - s0) * c.rb);
+        ++c.j;
+        return true;
+      }
+    } else if (c.u < c.units) {
+      const int j = c.u / c.nch, ch = c.u - j * c.nch;
+      const int t0 = ch * c.cl;
+      const int tend = min(t0 + c.cl, pos);  // the slot at pos is written in this step: never streamed
+      const int nk = tend > t0 ? tend - t0 : 0;
+      const size_t base = ((size_t)j * p.m.max_ctx + t0) * p.m.d;
+      src = (c.sub == 0 ? c.kc : c.vc) + base;
+      bytes = (uint32_t)(nk * p.m.d * 2);
+      if (c.sub) { c.sub = 0; c.u += p.grid; } else { c.sub = 1; }
+      return true;
+    }
+    ++c.k;
+    cursor_enter(p, c, pos);
+  }
+  return false;
+}
+
+// The persistent kernel's producer: feeds the ring in schedule order with bulk copies (at most
+// p.inflight outstanding). While the ring is full -- the consumers are in a latency-bound stretch
+// (barrier, attention, a small matrix) -- it walks a second cursor ahead and prefetches upcoming
+// stages into L2, paced at about this SM's share of HBM bandwidth and at most l2_lookahead bytes
+// beyond the copies, so that HBM keeps streaming while the ring cannot take more. Later copies of
+// those stages hit L2.
+__device__ __forceinline__ void produce_step(const StepParams& p, Pipe& pp, int pos,
+                                             unsigned long long* trace) {
+  const uint64_t pol_w = policy_evict_first(), pol_pf = policy_evict_normal();
+  StageCursor cp{}, pf{};
+  cp.k = 0;
+  cursor_enter(p, cp, pos);
+  pf = cp;
+  long long cend = 0, pend = 0;  // stream offsets: end of the current copy, end of prefetched bytes
+  uint64_t next_pf = 0;
+  bool dead = false;
+  const void* src;
+  uint32_t bytes;
+  const volatile int* done = &pp.ms->cons_done;
+  int last_k = -1;
+  while (!dead && cursor_next(p, cp, pos, src, bytes)) {
+    if (trace && cp.k != last_k) {  // timeline: the producer moves on to phase cp.k
+      const uint64_t t = globaltimer();
+      if (last_k >= 0) *trace_at(trace, p, last_k, TR_PROD_END) = t;
+      *trace_at(trace, p, cp.k, TR_PROD_BEGIN) = t;
+    }
+    last_k = cp.k;
+    cend += bytes;
+    const int s = pp.s;
+    const uint32_t eb = pp.empty0 + 8u * s;
+    if (!mbar_try_wait(eb, pp.ph ^ 1u)) {
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(eb, pp.ph ^ 1u)) {
+        if (*done) { dead = true; break; }
+        const uint64_t now = globaltimer();
+        if (p.l2_lookahead > 0 && now >= next_pf) {
+          // prefetch the next stage the copies have not reached, within the lookahead window
+          const void* ps = nullptr;
+          uint32_t pb = 0;
+          bool have = false;
+          while (pend < cend) {  // catch up with the copy cursor without prefetching
+            if (!cursor_next(p, pf, pos, ps, pb)) { pend = 1LL << 62; break; }
+            pend += pb;
+          }
+          if (pend >= cend && pend - cend < p.l2_lookahead && pend < (1LL << 62)) {
+            if (cursor_next(p, pf, pos, ps, pb)) { have = true; pend += pb; }
+            else pend = 1LL << 62;
+          }
+          if (have && pb) {
+            bulk_prefetch_l2(ps, pb, pol_pf);
+            next_pf = now + (uint64_t)pb * (uint64_t)p.l2_pace_ns_per_kb / 1024u;
+          }
+        }
+        if ((long long)(now - t0) > pp.timeout) {
+          dead = true;
+          if (!*done) raise_error(pp.err, pp.err_host, EW_TIMEOUT);
+          break;
+        }
+      }
+      if (dead) break;
+    }
+    if (pp.inflight > 0 && pp.it >= (uint32_t)pp.inflight) {
+      const int k = pp.inflight;
+      const int s2 = s >= k ? s - k : s - k + pp.stages;
+      const uint32_t p2 = s >= k ? pp.ph : pp.ph ^ 1u;
+      if (!mbar_try_wait(pp.full0 + 8u * s2, p2) &&
+          !wait_bar(pp.full0 + 8u * s2, p2, pp.timeout, &pp.ms->cons_done))
+        break;
+    }
+    const uint32_t fb = pp.full0 + 8u * s;
+    mbar_arrive_expect_tx(fb, bytes);
+    if (bytes) bulk_g2s(pp.ring + (uint32_t)s * pp.slot, src, bytes, fb, pol_w);
+    pipe_advance(pp);
+  }
+  if (trace && last_k >= 0) *trace_at(trace, p, last_k, TR_PROD_END) = globaltimer();
+  prod_drain(pp);
+}
+
+
+// Consumer side of one attention phase (every unit this CTA owns). Separate from the GEMV phase so
+// that each gets its own register allocation; the pipe state goes in and comes back by value.
+__device__ __forceinline__ Pipe consume_attn_phase(const StepParams& p, Pipe pp, int layer, int pos,
+                                                int tid, int k, unsigned long long* trace) {
+  unsigned long long* tr_ready = trace_at(trace, p, k, TR_READY);
+  if (tr_ready && tid == 0) *tr_ready = globaltimer();
+  const AttnArgs A = step_attn_args(p, layer, pos);
+  const AttnSplit sp = attn_split(pos, A.nkv, A.d, p.grid, p.slot_bytes, p.n_chunks_override);
+  const int units = A.nkv * sp.nch;
+  for (int u = blockIdx.x; u < units; u += p.grid) attn_unit(pp, A, sp, u / sp.nch, u % sp.nch, tid);
+  return pp;
+}
+
+// The plan of a GEMV phase: QKV (RMSNorm prologue, bias), O (+ residual), gate/up (RMSNorm,
+// SwiGLU), down (+ residual) or the LM head (final RMSNorm, logits, argmax).
+__device__ __forceinline__ GemvPlan plan_gemv(const StepParams& p, Pipe& pp, int phase, int layer,
+                                              int token, int tid) {
+  const Dims& m = p.m;
+  GemvPlan pl;
+  pl.g = phase_gemv(p, phase, layer);
+  pl.rs = row_split(pl.g, blockIdx.x, p.grid, p.slot_bytes);
+  const LayerDev& L = p.layers[layer];
+  pl.src = ActSrc{};
+  pl.src.eps = m.eps;
+  switch (phase) {
+    case PH_QKV:
+      if (layer == 0) pl.src.xb = p.embed + (size_t)token * m.H; else pl.src.xf = p.x;
+      pl.src.gf = L.g1; pl.src.n = m.H;
+      pl.epi = Epi{EK_STORE, p.qkv, L.bias};
+      break;
+    case PH_O:
+      pl.src.xf = p.attn; pl.src.n = m.nq * m.d;
+      pl.epi = Epi{EK_RESIDUAL, p.x, nullptr};
+      break;
+    case PH_GU:
+      pl.src.xf = p.x; pl.src.gf = L.g2; pl.src.n = m.H;
+      pl.epi = Epi{EK_SWIGLU, p.act, nullptr};
+      break;
+    case PH_DOWN:
+      pl.src.xf = p.act; pl.src.n = m.F;
+      pl.epi = Epi{EK_RESIDUAL, p.x, nullptr};
+      break;
+    default:
+      pl.src.xf = p.x; pl.src.gb = p.final_norm; pl.src.n = m.H;
+      pl.epi = Epi{EK_ARGMAX, p.logits, nullptr};
+      break;
+  }
+  gemv_plan_finish(pp, pl, tid);
+  return pl;
+}
+
+// Consumer side of one GEMV phase from its plan.
+template <int FMT, int NCHL>
+__device__ __forceinline__ void run_gemv_phase(const StepParams& p, Pipe& pp, const GemvPlan& pl,
+                                               int phase, int layer, int token, int tid, int k,
+                                               unsigned long long* trace) {
+  const Dims& m = p.m;
+  unsigned long long* tr_ready = trace_at(trace, p, k, TR_READY);
+  Best best{-CUDART_INF_F, 0x7FFFFFFF, 0};
+  // int4 models stream their linears as int4 and the LM head as bf16; bf16 models need one format
+  if (FMT == 1 && pl.g.fmt == 1) gemv_rows<1, 2>(pp, pl, best, tid, tr_ready);
+  else gemv_rows<0, NCHL>(pp, pl, best, tid, tr_ready);
+  if (phase == PH_QKV && layer == 0 && blockIdx.x == 0)
+    for (int i = tid; i < m.H; i += NCT) p.x[i] = bf16_to_f(p.embed[(size_t)token * m.H + i]);
+  if (phase == PH_LM) {
+    const Best cb = best_block_reduce(best, pp.ms, tid);
+    argmax_publish(cb, p.best_val, p.best_idx, p.best_bad, p.tickets + m.nkv, p.grid, blockIdx.x,
+                   p.argmax, p.err, p.err_host, pp.ms, tid);
+  }
+}
+
+// Phase k: its plan (GEMV phases) and its run. The persistent kernel calls plan_phase for phase
+// k + 1 before the grid barrier that ends phase k.
+__device__ __forceinline__ GemvPlan plan_phase(const StepParams& p, Pipe& pp, int k, int token,
+                                               int tid) {
+  int phase, layer;
+  phase_of(k, p.m.L, phase, layer);
+  if (phase == PH_ATTN) return GemvPlan{};
+  return plan_gemv(p, pp, phase, layer, token, tid);
+}
+
+template <int FMT, int NCHL>
+__device__ __forceinline__ void run_phase(const StepParams& p, Pipe& pp, const GemvPlan& pl, int k,
+                                          int token, int pos, int tid, unsigned long long* trace) {
+  int phase, layer;
+  phase_of(k, p.m.L, phase, layer);
+  if (phase == PH_ATTN) pp = consume_attn_phase(p, pp, layer, pos, tid, k, trace);
+  else run_gemv_phase<FMT, NCHL>(p, pp, pl, phase, layer, token, tid, k, trace);
+}
+
+// Barrier over the CTAs of the cooperative launch, run by the consumer warps: one monotonic
+// arrival counter (it never resets; barrier k of a launch waits for bar_base + (k+1) * grid).
+// It is split in two so that work which needs no other CTA's results (the next phase's plan) runs
+// between the arrival and the wait. grid_arrive: after all consumer threads are done, thread 0
+// arrives with a release reduction that publishes the CTA's writes. It returns, in thread 0, 0 when
+// it arrived, 1 when the step must stop, 2 when fault injection skipped the arrival.
+__device__ __forceinline__ int grid_arrive(const StepParams& p, Misc* ms, int tid, int index) {
+  named_sync(BAR_CONS, NCT);
+  int state = 0;
+  if (tid == 0) {
+    if (*reinterpret_cast<volatile int*>(&ms->abort)) state = 1;
+    else if (p.dbg_skip_cta == (int)blockIdx.x && p.dbg_skip_barrier == index) state = 2;
+    else red_add_release(p.gbar, 1u);
+  }
+  return state;
+}
+
+// grid_wait: thread 0 polls with acquire loads until the counter reaches the barrier's target,
+// under a time limit; the poll also ends when another CTA has raised an error. Returns false, the
+// same in every consumer thread, when the step must stop.
+__device__ __forceinline__ bool grid_wait(const StepParams& p, Misc* ms, int tid, int index, int state) {
+  if (tid == 0) {
+    int stop = state == 1;
+    if (state == 0) {
+      const unsigned target = p.bar_base + (unsigned)(index + 1) * (unsigned)p.grid;
+      const uint64_t t0 = globaltimer();
+      unsigned spins = 0;
+      while ((int)(ld_acquire(p.gbar) - target) < 0) {
+        if ((++spins & 63u) == 0) {
+          if (ld_volatile_int(p.err) != 0) { stop = 1; break; }
+          if ((long long)(globaltimer() - t0) > p.timeout_ns) {
+            raise_error(p.err, p.err_host, EW_TIMEOUT);
+            stop = 1;
+            break;
+          }
+        }
+      }
+    }
+    ms->exit_now = stop;
+  }
+  named_sync(BAR_CONS, NCT);
+  return !*reinterpret_cast<volatile int*>(&ms->exit_now);
+}
+
+// Start-of-step decision, identical in every CTA: skip when an earlier step left an error, or when
+// the token id is out of range (CTA 0 records that).
+__device__ __forceinline__ bool step_prologue(const StepParams& p, int& token, int pos, int* s_tok) {
+  if (threadIdx.x == 0) {
+    int e = ld_volatile_int(p.err);
+    const int tok = p.token_dev ? *p.token_dev : p.token;
+    if (e == 0 && (tok < 0 || tok >= p.m.V)) {
+      if (blockIdx.x == 0) raise_error(p.err, p.err_host, EW_BADTOKEN);
+      e = 1;
+    }
+    s_tok[0] = tok;
+    s_tok[1] = e;
+  }
+  __syncthreads();
+  token = s_tok[0];
+  (void)pos;
+  return s_tok[1] == 0;
+}
+
+template <int FMT, int NCHL, bool TRACE>
+__global__ void __launch_bounds__(NTHREADS_MEGA, 1) decode_megakernel(const __grid_constant__ StepParams p) {
+  unsigned long long* const trace = TRACE ? p.trace : nullptr;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ int s_tok[2];
+  Pipe pp;
+  pipe_init(pp, smem, p.ring_stages, p.slot_bytes, p.timeout_ns, p.err, p.err_host);
+  pp.inflight = p.inflight;
+  pipe_setup(pp);
+  int token = 0;
+  const int pos = p.pos;
+  if (!step_prologue(p, token, pos, s_tok)) return;
+  const int nph = p.m.L * PHASES_PER_LAYER + 1;
+  const int tid = threadIdx.x;
+  if (tid >= NCT) {
+    reg_dealloc<REG_PRODUCER>();
+    if (tid == NCT) produce_step(p, pp, pos, trace);
+  } else {
+    reg_alloc<REG_CONSUMER>();
+    GemvPlan plan = plan_phase(p, pp, 0, token, tid);
+    for (int k = 0; k < nph; ++k) {
+      if (unsigned long long* t = trace_at(trace, p, k, TR_START)) if (tid == 0) *t = globaltimer();
+      run_phase<FMT, NCHL>(p, pp, plan, k, token, pos, tid, trace);
+      if (unsigned long long* t = trace_at(trace, p, k, TR_END)) if (tid == 0) *t = globaltimer();
+      if (k + 1 < nph) {
+        const int st = grid_arrive(p, pp.ms, tid, k);
+        plan = plan_phase(p, pp, k + 1, token, tid);  // overlaps the barrier wait
+        if (!grid_wait(p, pp.ms, tid, k, st)) break;
+      }
+    }
+    if (tid == 0) *reinterpret_cast<volatile int*>(&pp.ms->cons_done) = 1;
+  }
+  __syncthreads();
+}
+
+template <int FMT, int NCHL>
+__global__ void __launch_bounds__(NTHREADS, 2) decode_phase_kernel(const __grid_constant__ StepParams p, int k) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  Pipe pp;
+  pipe_init(pp, smem, p.ring_stages, p.slot_bytes, p.timeout_ns, p.err, p.err_host);
+  pp.inflight = p.inflight;
+  pipe_setup(pp);
+  __syncthreads();
+  pdl_launch_dependents();
+  int phase, layer;
+  phase_of(k, p.m.L, phase, layer);
+  const int tid = threadIdx.x;
+  if (tid >= NCT) {
+    if (tid == NCT) {
+      // the step block was written by the step's first node, which completed before this grid
+      // could start; only the attention producer needs pos
+      const int pos = phase == PH_ATTN ? p.step_dev[1] : 0;
+      bool dead = false;
+      produce_phase(p, pp, phase, layer, pos, policy_evict_first(), policy_evict_normal(), dead);
+      prod_drain(pp);
+    }
+  } else {
+    pdl_wait();
+    if (tid == 0) pp.ms->exit_now = ld_volatile_int(p.err) != 0;
+    named_sync(BAR_CONS, NCT);
+    if (!*reinterpret_cast<volatile int*>(&pp.ms->exit_now)) {
+      const int token = p.step_dev[0], pos = p.step_dev[1];
+      const GemvPlan plan = plan_phase(p, pp, k, token, tid);  // after the wait: reads x of the previous kernel
+      run_phase<FMT, NCHL>(p, pp, plan, k, token, pos, tid, p.trace);
+    }
+    named_sync(BAR_CONS, NCT);
+    if (tid == 0) *reinterpret_cast<volatile int*>(&pp.ms->cons_done) = 1;
+  }
+  __syncthreads();
+}
+
+
+// The instances one translation unit provides for its weight format (see mega_bf16.cu and
+// mega_int4.cu): nchl is 4, 6 or 8.
+#define TINFER_MEGA_INSTANCES(FMT, NAME)                                                        \
+  const void* NAME(int nchl, int kind) {                                                        \
+    switch (nchl * 4 + kind) {                                                                  \
+      case 16: return reinterpret_cast<const void*>(&decode_megakernel<FMT, 4, false>);         \
+      case 17: return reinterpret_cast<const void*>(&decode_megakernel<FMT, 4, true>);          \
+      case 18: return reinterpret_cast<const void*>(&decode_phase_kernel<FMT, 4>);              \
+      case 24: return reinterpret_cast<const void*>(&decode_megakernel<FMT, 6, false>);         \
+      case 25: return reinterpret_cast<const void*>(&decode_megakernel<FMT, 6, true>);          \
+      case 26: return reinterpret_cast<const void*>(&decode_phase_kernel<FMT, 6>);              \
+      case 32: return reinterpret_cast<const void*>(&decode_megakernel<FMT, 8, false>);         \
+      case 33: return reinterpret_cast<const void*>(&decode_megakernel<FMT, 8, true>);          \
+      case 34: return reinterpret_cast<const void*>(&decode_phase_kernel<FMT, 8>);              \
+      default: return nullptr;                                                                  \
+    }                                                                                           \
+  }
+
+}  // namespace tinfer

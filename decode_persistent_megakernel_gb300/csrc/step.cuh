@@ -149,7 +149,7 @@ __device__ __forceinline__ void prod_push(Pipe& pp, const void* src, uint32_t by
 }
 
 // Before the CTA exits: every copy this producer issued has landed (bounded wait).
-__device__ void prod_drain(Pipe& pp) {
+static __device__ void prod_drain(Pipe& pp) {
   const uint32_t n = pp.it < (uint32_t)pp.stages ? pp.it : (uint32_t)pp.stages;
   int never = 0;
   for (uint32_t k = pp.it - n; k < pp.it; ++k)
@@ -271,7 +271,7 @@ __device__ __forceinline__ float2 dot8_bf16(const uint4 w, const float* a, float
 // product is rounded exactly as q * a would be. Pairs go through Blackwell's packed f32x2 units.
 __device__ __forceinline__ float dot32_int4(const uint4 w, const float* a) {
   constexpr uint32_t MAG = 0x4B000000u;
-  const float2 B = make_float2(8388608.f, 8388608.f);
+  const float2 B = make_float2(-8388608.f, -8388608.f);
   float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
   const uint32_t words[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -281,10 +281,10 @@ __device__ __forceinline__ float dot32_int4(const uint4 w, const float* a) {
     const float2 f23 = make_float2(__uint_as_float((lo & 0x0F00u) | MAG), __uint_as_float((lo & 0xF000u) | MAG));
     const float2 f45 = make_float2(__uint_as_float((hi & 0x000Fu) | MAG), __uint_as_float((hi & 0x00F0u) | MAG));
     const float2 f67 = make_float2(__uint_as_float((hi & 0x0F00u) | MAG), __uint_as_float((hi & 0xF000u) | MAG));
-    acc0 = fma2(sub2(f01, B), make_float2(a[8 * k + 0], a[8 * k + 1]), acc0);
-    acc1 = fma2(sub2(f23, B), make_float2(a[8 * k + 2], a[8 * k + 3]), acc1);
-    acc0 = fma2(sub2(f45, B), make_float2(a[8 * k + 4], a[8 * k + 5]), acc0);
-    acc1 = fma2(sub2(f67, B), make_float2(a[8 * k + 6], a[8 * k + 7]), acc1);
+    acc0 = fma2(add2(f01, B), make_float2(a[8 * k + 0], a[8 * k + 1]), acc0);
+    acc1 = fma2(add2(f23, B), make_float2(a[8 * k + 2], a[8 * k + 3]), acc1);
+    acc0 = fma2(add2(f45, B), make_float2(a[8 * k + 4], a[8 * k + 5]), acc0);
+    acc1 = fma2(add2(f67, B), make_float2(a[8 * k + 6], a[8 * k + 7]), acc1);
   }
   return (acc0.x + acc0.y) + (acc1.x + acc1.y);
 }
@@ -312,9 +312,9 @@ struct RowSplit {
   int r0, r1, nr;
 };
 __device__ __forceinline__ RowSplit row_split(const GemvDesc& g, int cta, int grid, int slot) {
-  const int units = g.rows / g.quantum;
-  const int u0 = (int)((long long)units * cta / grid);
-  const int u1 = (int)((long long)units * (cta + 1) / grid);
+  const unsigned units = (unsigned)(g.rows / g.quantum);  // units * grid < 2^32 for every model here
+  const int u0 = (int)(units * (unsigned)cta / (unsigned)grid);
+  const int u1 = (int)(units * (unsigned)(cta + 1) / (unsigned)grid);
   return RowSplit{u0 * g.quantum, u1 * g.quantum, stage_rows(g.fmt, g.cols, g.rb, slot, g.quantum)};
 }
 
@@ -384,31 +384,58 @@ __device__ __forceinline__ void vec8(const Pipe& pp, bool f32, int i, float* o) 
 // butterfly reduction. The LM head applies its epilogue in the warp; every other matrix leaves its
 // per-segment row results in shared memory, and one pass at the end of the phase sums the
 // segments in a fixed order and applies the epilogue (bias, residual add, SwiGLU on gate/up pairs).
+// Everything a GEMV phase needs that does not depend on other CTAs' results of the previous phase.
+// The persistent kernel builds it before the grid barrier, so that its cost (descriptors, the row
+// split, cold code, the residual or bias operand and the wait for the gain stage) hides under the
+// barrier wait instead of adding to the phase.
+struct GemvPlan {
+  GemvDesc g;
+  RowSplit rs;
+  ActSrc src;
+  Epi epi;
+  float pre;     // epilogue operand of row rs.r0 + tid (residual x or bias), fetched early
+  uint32_t gs;   // shared address of the phase's gain stage (RMSNorm phases), already acquired
+};
+
+// Completes a plan whose g, rs, src and epi are set: loads the early epilogue operand (the residual
+// rows are this CTA's own from its previous write, or the constant bias) and acquires the gain stage.
+__device__ __forceinline__ void gemv_plan_finish(Pipe& pp, GemvPlan& pl, int tid) {
+  const SegInfo si = seg_info(pl.g.fmt, pl.g.cols);
+  const int nrows = pl.rs.r1 - pl.rs.r0;
+  const bool direct = pl.epi.kind == EK_ARGMAX && si.nseg == 1;
+  pl.pre = 0.f;
+  if (!direct && tid < nrows && pl.epi.kind != EK_ARGMAX) {
+    if (pl.epi.kind == EK_RESIDUAL) pl.pre = __ldcg(pl.epi.y + pl.rs.r0 + tid);
+    else if (pl.epi.kind == EK_STORE && pl.epi.bias) pl.pre = __ldg(pl.epi.bias + pl.rs.r0 + tid);
+  }
+  pl.gs = (pl.src.gf || pl.src.gb) ? cons_acquire(pp) : 0u;
+}
+
 template <int FMT, int NCHL>
-__device__ void gemv_rows(Pipe& pp, const GemvDesc& g, const RowSplit& rs, const ActSrc& src,
-                          const Epi& epi, Best& best, int tid, unsigned long long* tr_ready) {
+__device__ void gemv_rows(Pipe& pp, const GemvPlan& pl, Best& best, int tid,
+                          unsigned long long* tr_ready) {
   constexpr int E = FMT == 0 ? 8 : 32;
+  const GemvDesc& g = pl.g;
+  const RowSplit& rs = pl.rs;
+  const ActSrc& src = pl.src;
+  const Epi& epi = pl.epi;
   Misc* ms = pp.ms;
   const int lane = tid & 31, warp = tid >> 5;
   const SegInfo si = seg_info(FMT, g.cols);
-  const int nchl = (si.chs + 31) / 32;  // chunks per lane actually used (<= NCHL)
+  const int nchl = (si.chs + 31) / 32;  // chunks per lane that hold inputs (<= NCHL)
   const int seg = warp % si.nseg, grp = warp / si.nseg, WG = NCW / si.nseg;
   const int nrows = rs.r1 - rs.r0;
   const bool direct = epi.kind == EK_ARGMAX && si.nseg == 1;  // the warp holds whole rows
   const bool norm = src.gf || src.gb;
-
-  // operands of the end-of-phase epilogue, fetched now so that their latency overlaps
-  float pre = 0.f;
-  if (!direct && tid < nrows && epi.kind != EK_ARGMAX) {
-    if (epi.kind == EK_RESIDUAL) pre = __ldcg(epi.y + rs.r0 + tid);
-    else if (epi.kind == EK_STORE && epi.bias) pre = __ldg(epi.bias + rs.r0 + tid);
-  }
+  const float pre = pl.pre;
 
   // activations of this warp's segment from the shared-memory copy of the input vector; chunks
   // past the segment read the last valid chunk and are zeroed, so that the row loop needs no
   // per-lane branches
+  if (tr_ready && tid == 0) tr_ready[TR_ENTRY - TR_READY] = globaltimer();
   fetch_vector(pp, src.xf ? (const void*)src.xf : (const void*)src.xb,
                (uint32_t)src.n * (src.xf ? 4u : 2u), tid);
+  if (tr_ready && tid == 0) tr_ready[TR_FETCHED - TR_READY] = globaltimer();
   float a[NCHL][E];
   float S[NCHL];
   float ss = 0.f;
@@ -419,10 +446,10 @@ __device__ void gemv_rows(Pipe& pp, const GemvDesc& g, const RowSplit& rs, const
     const bool ok = lane + 32 * k < si.chs;
 #pragma unroll
     for (int e = 0; e < E; e += 8) {
-      if (k < nchl) vec8(pp, src.xf != nullptr, base + e, &a[k][e]);
+      vec8(pp, src.xf != nullptr, base + e, &a[k][e]);  // clamped chunk: always a valid address
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        a[k][e + u] = (ok && k < nchl) ? a[k][e + u] : 0.f;
+        a[k][e + u] = ok ? a[k][e + u] : 0.f;
         ss = fmaf(a[k][e + u], a[k][e + u], ss);
       }
     }
@@ -438,10 +465,10 @@ __device__ void gemv_rows(Pipe& pp, const GemvDesc& g, const RowSplit& rs, const
     }
     const float inv = 1.f / sqrtf(tot / (float)src.n + src.eps);
     // the gain vector is the phase's first ring stage (fp32, or bf16 for the final norm)
-    const uint32_t gs = cons_acquire(pp);
+    const uint32_t gs = pl.gs;
 #pragma unroll
     for (int k = 0; k < NCHL; ++k) {
-      if (k < nchl) {
+      {
         const int c = min(lane + 32 * k, si.chs - 1);
         const int base = seg * si.ks + c * E;
 #pragma unroll
@@ -482,24 +509,30 @@ __device__ void gemv_rows(Pipe& pp, const GemvDesc& g, const RowSplit& rs, const
 
   const uint32_t seg_off = FMT == 0 ? (uint32_t)(seg * si.ks * 2) : (uint32_t)(seg * si.ks / 2);
   const uint32_t scale_off = (uint32_t)(g.cols / 2);
-  const int lane_c = lane;  // chunk k of this lane is lane + 32 k, clamped to the segment
+  // byte offsets inside a row of this lane's chunks (chunk k = lane + 32 k, clamped) and scales
+  uint32_t coff[NCHL], soff[NCHL];
+#pragma unroll
+  for (int k = 0; k < NCHL; ++k) {
+    const int c = min(lane + 32 * k, si.chs - 1);
+    coff[k] = seg_off + (uint32_t)c * 16u;
+    soff[k] = FMT == 1 ? scale_off + 2u * (uint32_t)((seg * si.ks + c * 32) / g.group) : 0u;
+  }
 
   // The warp walks its rows stage by stage (rows grp, grp + WG, ... of each stage). Lane partials
   // of the last eight rows ride in a shift window; a full window is finished by one transposed
-  // reduction (9 shuffles for 8 rows). A stage is released as soon as the warp's last row in it
-  // has been read.
+  // reduction (9 shuffles for 8 rows). Row ids follow from the warp's row counter: its n-th row is
+  // row (n / m) * nr + grp + (n % m) * WG of the CTA's slice, m rows per full stage. A stage is
+  // released as soon as the warp's last row in it has been read.
+  const int m = rs.nr > grp ? (rs.nr - grp + WG - 1) / WG : 0;
   float w0 = 0.f, w1 = 0.f, w2 = 0.f, w3 = 0.f, w4 = 0.f, w5 = 0.f, w6 = 0.f, w7 = 0.f;
-  int r0 = -1, r1 = -1, r2 = -1, r3 = -1, r4 = -1, r5 = -1, r6 = -1, r7 = -1;
-  int filled = 0;
+  int nrow = 0, filled = 0;
   auto flush = [&]() {
     const float part[8] = {w0, w1, w2, w3, w4, w5, w6, w7};
-    const int rid[8] = {r0, r1, r2, r3, r4, r5, r6, r7};
     const float v = transpose_reduce8(part, lane);
     const int q8 = transpose_row8(lane);
-    int rl = -1;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) rl = q == q8 ? rid[q] : rl;
-    if ((lane & 3) == 0 && rl >= 0) {
+    if ((lane & 3) == 0 && q8 < filled) {
+      const int n = nrow - 1 - q8;  // slot q holds the warp's row nrow - 1 - q
+      const int rl = (n / m) * rs.nr + grp + (n % m) * WG;
       if (direct) {
         const int r = rs.r0 + rl;
         if (epi.y) epi.y[r] = v;
@@ -509,7 +542,6 @@ __device__ void gemv_rows(Pipe& pp, const GemvDesc& g, const RowSplit& rs, const
       }
     }
     w0 = w1 = w2 = w3 = w4 = w5 = w6 = w7 = 0.f;
-    r0 = r1 = r2 = r3 = r4 = r5 = r6 = r7 = -1;
     filled = 0;
   };
   for (int s0 = rs.r0; s0 < rs.r1; s0 += rs.nr) {
@@ -519,27 +551,27 @@ __device__ void gemv_rows(Pipe& pp, const GemvDesc& g, const RowSplit& rs, const
     for (int i = grp; i < nrs; i += WG) {
       const uint32_t rowp = st + (uint32_t)i * g.rb;
       float2 acc = make_float2(0.f, 0.f), acc2 = make_float2(0.f, 0.f);
+      // every chunk is loaded unconditionally (clamped offsets, zero activations past the row), so
+      // that all loads of the row issue back to back
+      uint4 wv[NCHL];
+#pragma unroll
+      for (int k = 0; k < NCHL; ++k) wv[k] = lds128(rowp + coff[k]);
 #pragma unroll
       for (int k = 0; k < NCHL; ++k) {
-        if (k < nchl) {
-          const int c = min(lane_c + 32 * k, si.chs - 1);
-          const uint4 w = lds128(rowp + seg_off + (uint32_t)c * 16u);
-          if (FMT == 0) {
-            if (k & 1) acc2 = dot8_bf16(w, a[k], acc2);
-            else acc = dot8_bf16(w, a[k], acc);
-          } else {
-            const float dq = dot32_int4(w, a[k]);
-            const uint16_t sb = lds16(rowp + scale_off + 2u * (uint32_t)((seg * si.ks + c * 32) / g.group));
-            const float sc = g.scale_bf16 ? bf16_to_f(sb) : __half2float(__ushort_as_half(sb));
-            acc.x = fmaf(sc, dq - 8.f * S[k], acc.x);
-          }
+        if (FMT == 0) {
+          if (k & 1) acc2 = dot8_bf16(wv[k], a[k], acc2);
+          else acc = dot8_bf16(wv[k], a[k], acc);
+        } else {
+          const float dq = dot32_int4(wv[k], a[k]);
+          const uint16_t sb = lds16(rowp + soff[k]);
+          const float sc = g.scale_bf16 ? bf16_to_f(sb) : __half2float(__ushort_as_half(sb));
+          acc.x = fmaf(sc, dq - 8.f * S[k], acc.x);
         }
       }
       // shift the window: the newest row enters at w0
       w7 = w6; w6 = w5; w5 = w4; w4 = w3; w3 = w2; w2 = w1; w1 = w0;
-      r7 = r6; r6 = r5; r5 = r4; r4 = r3; r3 = r2; r2 = r1; r1 = r0;
       w0 = (acc.x + acc.y) + (acc2.x + acc2.y);
-      r0 = (s0 - rs.r0) + i;
+      ++nrow;
       if (++filled == 8) flush();
     }
     cons_release(pp, lane);
@@ -571,12 +603,18 @@ __device__ void gemv_rows(Pipe& pp, const GemvDesc& g, const RowSplit& rs, const
   }
 }
 
-// Dispatch to the instance of the weight format (the chunk count per lane is a runtime bound).
-__device__ __forceinline__ void gemv_consume_any(Pipe& pp, const GemvDesc& g, const RowSplit& rs,
-                                                 const ActSrc& src, const Epi& epi, Best& best,
-                                                 int tid, unsigned long long* tr_ready) {
-  if (g.fmt == 1) gemv_rows<1, 2>(pp, g, rs, src, epi, best, tid, tr_ready);
-  else gemv_rows<0, 8>(pp, g, rs, src, epi, best, tid, tr_ready);
+// Dispatch to the instance of the weight format and chunk count per lane (rounded up to even).
+__device__ __forceinline__ void gemv_consume_any(Pipe& pp, const GemvPlan& pl, Best& best, int tid,
+                                                 unsigned long long* tr_ready) {
+  if (pl.g.fmt == 1) {
+    gemv_rows<1, 2>(pp, pl, best, tid, tr_ready);
+    return;
+  }
+  const int nchl = (seg_info(0, pl.g.cols).chs + 31) / 32;
+  if (nchl > 6) gemv_rows<0, 8>(pp, pl, best, tid, tr_ready);
+  else if (nchl > 4) gemv_rows<0, 6>(pp, pl, best, tid, tr_ready);
+  else if (nchl > 2) gemv_rows<0, 4>(pp, pl, best, tid, tr_ready);
+  else gemv_rows<0, 2>(pp, pl, best, tid, tr_ready);
 }
 
 __device__ __forceinline__ void produce_rows(Pipe& pp, const GemvDesc& g, const RowSplit& rs,
@@ -616,7 +654,7 @@ __device__ __forceinline__ Best best_block_reduce(Best b, Misc* ms, int tid) {
 // combines all slots (order-independent: max value, then lowest index) and writes the token, or -1
 // and the non-finite error bit ("Decoding in tiles", section 5: per-task best candidates, lowest
 // token id among ties, an error word on a non-finite logit).
-__device__ void argmax_publish(const Best& mine, float* slot_v, int* slot_i, int* slot_bad,
+static __device__ void argmax_publish(const Best& mine, float* slot_v, int* slot_i, int* slot_bad,
                                unsigned* ticket, int nslots, int cta, int* out, int* err,
                                int* err_host, Misc* ms, int tid) {
   if (tid == 0) {
@@ -708,7 +746,7 @@ __device__ __forceinline__ void produce_attn_unit(Pipe& pp, const AttnArgs& A, i
 // Merge of one KV head's chunk partials for its query heads (the log-sum-exp combine). Warp g finds
 // head g's maximum and weights (lanes over chunks), then each output element sums its chunks'
 // unnormalised outputs in a fixed order, eight loads in flight at a time.
-__device__ void attn_merge(const AttnArgs& A, Misc* ms, int tid, int j, int nch) {
+static __device__ void attn_merge(const AttnArgs& A, Misc* ms, int tid, int j, int nch) {
   const int G = A.nq / A.nkv, d = A.d;
   const int warp = tid >> 5, lane = tid & 31;
   if (warp < G) {
@@ -750,7 +788,7 @@ __device__ void attn_merge(const AttnArgs& A, Misc* ms, int tid, int j, int nch)
 // per-head max / exponentials / sum, the value sum, and the partial (m, l, o) of the chunk
 // ("One launch per token", "The attention trap"; tinyinfer, "Round 2": one block per KV head and
 // chunk serving all grouped query heads, K/V read once). The last CTA done with head j merges.
-__device__ void attn_unit(Pipe& pp, const AttnArgs& A, const AttnSplit& sp, int j, int c, int tid) {
+static __device__ void attn_unit(Pipe& pp, const AttnArgs& A, const AttnSplit& sp, int j, int c, int tid) {
   Misc* ms = pp.ms;
   const int lane = tid & 31, warp = tid >> 5;
   const int d = A.d, half = d / 2, G = A.nq / A.nkv;
