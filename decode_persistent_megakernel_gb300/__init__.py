@@ -20,13 +20,14 @@ TINFER_MEGAKERNEL, TINFER_GRAPH = 0, 1
 TINFER_Q_GRID, TINFER_Q_SMEM, TINFER_Q_RING_STAGES, TINFER_Q_SLOT_BYTES, TINFER_Q_KERNELS_PER_STEP, \
     TINFER_Q_TRACE_BYTES = range(6)
 TINFER_EPI_STORE, TINFER_EPI_RESIDUAL, TINFER_EPI_SWIGLU, TINFER_EPI_ARGMAX = range(4)
+TINFER_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 EXPORTS = [
     "tinfer_status_string", "tinfer_check_config", "tinfer_packed_layer_bytes", "tinfer_pack_layer",
     "tinfer_unpack_layer", "tinfer_create", "tinfer_decode_step", "tinfer_decode_step_dev",
     "tinfer_generate", "tinfer_get_error", "tinfer_query", "tinfer_set_trace", "tinfer_set_timeout_ns",
     "tinfer_debug_skip_barrier", "tinfer_destroy", "tinfer_packed_row_bytes", "tinfer_pack_matrix",
-    "tinfer_op_gemv", "tinfer_op_attention",
+    "tinfer_op_gemv", "tinfer_op_attention", "tinfer_op_attention_noalloc",
 ]
 
 
@@ -92,6 +93,7 @@ def lib():
             "tinfer_pack_matrix": ([I, I, I, I, I, P, P, P, P], I),
             "tinfer_op_gemv": ([I, I, I, I, I, P, P, P, D, P, I, P, P, P], I),
             "tinfer_op_attention": ([I, I, I, I, D, I, I, P, P, P, P, P, P, P, P], I),
+            "tinfer_op_attention_noalloc": ([I, I, I, I, D, I, I, P, P, P, P, P], I),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -214,6 +216,13 @@ def tinfer_op_attention(nq, nkv, d, max_ctx, theta, pos, n_chunks, qkv, k_layer,
     return lib().tinfer_op_attention(nq, nkv, d, max_ctx, float(theta), pos, n_chunks, _ptr(qkv),
                                      _ptr(k_layer), _ptr(v_layer), _ptr(out), _ptr(part_m),
                                      _ptr(part_l), _ptr(part_o), _stream(stream))
+
+
+def tinfer_op_attention_noalloc(nq, nkv, d, max_ctx, theta, pos, n_chunks, qkv, k_layer, v_layer,
+                                out, stream=None) -> int:
+    return lib().tinfer_op_attention_noalloc(nq, nkv, d, max_ctx, float(theta), pos, n_chunks,
+                                             _ptr(qkv), _ptr(k_layer), _ptr(v_layer), _ptr(out),
+                                             _stream(stream))
 
 
 # ------------------------------------------------------------------ marshalling helpers

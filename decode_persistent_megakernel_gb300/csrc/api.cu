@@ -3,7 +3,9 @@
 
 #include <cmath>
 #include <cstdlib>
+#include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -755,3 +757,86 @@ tinfer_status tinfer_op_attention(int nq, int nkv, int d, int max_ctx, double th
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------- attention without allocation
+// The scratch of tinfer_op_attention_noalloc: a fixed array in the library's device image, so that
+// the call never allocates. Layout: [0, 256) error word; [256, 1280) merge tickets (one word per KV
+// head); [1280, 2048) the cos/sin row of pos; [2048, end) chunk partials m, l, o.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[TINFER_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr size_t NA_ERR = 0, NA_TICKETS = 256, NA_ROPE = 1280, NA_PARTS = 2048;
+
+// Device address of the scratch array, looked up once per device (with that device current) and
+// kept; later calls on the device only read the table.
+tinfer_status noalloc_scratch(unsigned char** base) {
+  static unsigned char* addr[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  TRY_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return TINFER_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return from_cuda(e);
+    addr[dev] = static_cast<unsigned char*>(p);
+  }
+  *base = addr[dev];
+  return TINFER_OK;
+}
+}  // namespace
+
+extern "C" tinfer_status tinfer_op_attention_noalloc(int nq, int nkv, int d, int max_ctx,
+                                                     double theta, int pos, int n_chunks,
+                                                     const float* qkv_dev, void* k_layer_dev,
+                                                     void* v_layer_dev, float* out_dev,
+                                                     void* stream) {
+  if (nq <= 0 || nkv <= 0 || nq % nkv || nq / nkv > G_MAX || d % 8 || d > D_MAX || max_ctx <= 0)
+    return TINFER_ERR_INVALID_ARG;
+  if (pos < 0 || pos >= max_ctx || !qkv_dev || !k_layer_dev || !v_layer_dev || !out_dev)
+    return TINFER_ERR_INVALID_ARG;
+  const int slot = SLOT_MIN;
+  int tmax = slot / (2 * d);
+  if (tmax > T_MAX) tmax = T_MAX;
+  const int grid = op_grid(1 << 30);
+  int nch = n_chunks;
+  if (nch <= 0) nch = nch_capacity(pos + 1, nkv, d, grid, slot);
+  if (nch > T_MAX || (pos + nch) / nch > tmax) return TINFER_ERR_UNSUPPORTED;  // ceil((pos+1)/nch)
+  // the fixed scratch bounds the problem: tickets and partials must fit their regions
+  const size_t part_floats = (size_t)nq * nch * (d + 2);
+  if ((size_t)nkv * 4 > NA_ROPE - NA_TICKETS || part_floats * 4 > TINFER_NOALLOC_SCRATCH_BYTES - NA_PARTS)
+    return TINFER_ERR_UNSUPPORTED;
+  unsigned char* base = nullptr;
+  TRY(noalloc_scratch(&base));
+  cudaStream_t st = (cudaStream_t)stream;
+
+  // cos/sin of position pos only (same formula and rounding as the engine's table); the kernel
+  // indexes the table by pos, so it gets a base address that puts row pos on the scratch row
+  const int half = d / 2;
+  float2 row[D_MAX / 2];
+  for (int i = 0; i < half; ++i) {
+    const double ang = (double)pos * std::pow(theta, -2.0 * (double)i / (double)d);
+    row[i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+  }
+  const uintptr_t rope_row = reinterpret_cast<uintptr_t>(base + NA_ROPE);
+  TRY_CUDA(cudaMemsetAsync(base, 0, NA_ROPE, st));  // error word and tickets start at zero
+  TRY_CUDA(cudaMemcpyAsync(base + NA_ROPE, row, sizeof(float2) * half, cudaMemcpyHostToDevice, st));
+
+  float* parts = reinterpret_cast<float*>(base + NA_PARTS);
+  OpAttnParams q{};
+  q.qkv = qkv_dev; q.kc = (uint16_t*)k_layer_dev; q.vc = (uint16_t*)v_layer_dev;
+  q.rope = reinterpret_cast<const float2*>(rope_row - (uintptr_t)pos * half * sizeof(float2));
+  q.part_m = parts; q.part_l = parts + (size_t)nq * nch; q.part_o = parts + (size_t)2 * nq * nch;
+  q.nch_cap = nch; q.tickets = reinterpret_cast<unsigned*>(base + NA_TICKETS); q.out = out_dev;
+  q.nq = nq; q.nkv = nkv; q.d = d; q.max_ctx = max_ctx; q.pos = pos; q.n_chunks = nch;
+  q.err = reinterpret_cast<int*>(base + NA_ERR); q.stages = 4; q.slot = slot;
+  q.timeout_ns = DEFAULT_TIMEOUT_NS;
+  const size_t smem = smem_for(4, slot, 0);
+  TRY_CUDA(set_smem_op_attention(smem));
+  TRY_CUDA(launch_op_attention(q, grid, smem, st));
+  TRY_CUDA(cudaStreamSynchronize(st));
+  int w = 0;
+  TRY_CUDA(cudaMemcpy(&w, base + NA_ERR, 4, cudaMemcpyDeviceToHost));
+  return w ? status_of_word(w) : TINFER_OK;
+}

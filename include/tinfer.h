@@ -202,6 +202,36 @@ tinfer_status tinfer_op_attention(int n_heads, int n_kv_heads, int head_dim, int
                                   float* part_m_dev, float* part_l_dev, float* part_o_dev,
                                   void* stream);
 
+/* ---------------------------------------------------------------------------------------------
+ * Attention that allocates nothing. The pages have no counterpart of this call: it is an
+ * engineering addition for embedders.
+ *
+ * Same operation, arguments, layouts and results as tinfer_op_attention with the optional partial
+ * outputs left out. The difference: the call allocates no device memory. Its working set (the
+ * RoPE row of pos, the per-KV-head merge tickets, the error word and the chunk partials) lives in
+ * one scratch array of TINFER_NOALLOC_SCRATCH_BYTES compiled into the library, one per device.
+ * It exists for callers that cannot allocate while they run: a serving process that has handed
+ * the rest of device memory to its KV pool (a cudaMalloc would fail there), or one that must not
+ * let a cudaMalloc / cudaFree synchronise the device under its other streams.
+ *
+ * - Size limit: n_kv_heads <= 256 and n_heads * n_chunks * (head_dim + 2) * 4 bytes <=
+ *   TINFER_NOALLOC_SCRATCH_BYTES - 2048 (n_chunks as chosen when 0 is passed). A call beyond it
+ *   returns TINFER_ERR_UNSUPPORTED before touching the device.
+ * - Set-up: the first call on a device, made with that device current, looks up the scratch
+ *   array's address (cudaGetSymbolAddress) and keeps it; make that first call before any stream
+ *   capture begins.
+ * - Each call clears the error word and the tickets on `stream` before its launch.
+ * - The scratch is shared by every call on a device: calls that overlap in time (other streams,
+ *   other host threads) race on it and must be serialised by the caller.
+ * - Synchronises `stream` before returning; device-side failures come back as the status
+ *   (TINFER_ERR_TIMEOUT, TINFER_ERR_NONFINITE) exactly as for tinfer_op_attention.
+ * --------------------------------------------------------------------------------------------- */
+#define TINFER_NOALLOC_SCRATCH_BYTES (1u << 20)
+tinfer_status tinfer_op_attention_noalloc(int n_heads, int n_kv_heads, int head_dim, int max_ctx,
+                                          double rope_theta, int pos, int n_chunks,
+                                          const float* qkv_dev, void* k_layer_dev,
+                                          void* v_layer_dev, float* out_dev, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
