@@ -45,6 +45,39 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+KERNEL_SOURCES = ["megakernel.cuh", "step.cuh", "ptx.cuh", "engine.h", "kernels.h", "mega_bf16.cu",
+                  "mega_int4.cu"]
+
+
+def kernel_source_hash() -> str:
+    """sha256 over the device-code sources of the step kernels (names and contents)."""
+    import hashlib
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "decode_persistent_megakernel_gb300", "csrc")
+    for name in KERNEL_SOURCES:
+        h.update(name.encode())
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes (read + write) per launch from the committed ncu summary of this kernel and
+    workload, or None when there is none or the kernel sources changed since it was taken."""
+    p = os.path.join(ROOT, "profiles", f"{kernel}_{workload}_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    kv = {}
+    with open(p) as f:
+        for ln in f:
+            if "=" in ln and not ln.lstrip().startswith("#"):
+                k, v = ln.split("=", 1)
+                kv[k.strip()] = v.strip()
+    if kv.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    return int(kv["dram_bytes_per_launch"])
+
+
 def algorithmic_bytes(c: dict, pos: int) -> int:
     """Bytes one step must move at position pos: every weight once in its stored format (linears,
     norms, biases, int4 scales), the LM head once, one embedding row, the K/V cache read over
@@ -254,6 +287,7 @@ def main():
         results[name] = dict(ms_total=ms_max, ms_step=ms_max / args.steps, clocks=clk.summary(),
                              launches=args.steps * eng.query(T.TINFER_Q_KERNELS_PER_STEP),
                              grid=eng.query(T.TINFER_Q_GRID), smem=eng.query(T.TINFER_Q_SMEM),
+                             threads=eng.query(T.TINFER_Q_BLOCK_THREADS),
                              stages=eng.query(T.TINFER_Q_RING_STAGES), slot=eng.query(T.TINFER_Q_SLOT_BYTES))
         if name == modes[0][0]:
             # end to end through the public call: host-in-the-loop greedy generation, one pinned
@@ -327,7 +361,8 @@ def main():
         "bytes_per_step": bytes_step,
         "floor_frac_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak,
+                     "traffic": measured_traffic("decode_megakernel", args.config) if main_mode == "mega" else None,
                      "kernel": "decode_megakernel" if main_mode == "mega" else "whole graph",
                      "peak_kind": peak_kind},
         "read_probe_gbs": read_gbs,
@@ -336,7 +371,7 @@ def main():
                 "d2h_bytes_per_step": 4},
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
-        "launch": {"grid": r["grid"], "threads": 288, "smem": r["smem"], "ring_stages": r["stages"],
+        "launch": {"grid": r["grid"], "threads": r["threads"], "smem": r["smem"], "ring_stages": r["stages"],
                    "slot_bytes": r["slot"]},
     }
     if "graph" in results and main_mode == "mega":

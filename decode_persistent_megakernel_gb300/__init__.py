@@ -18,7 +18,7 @@ TINFER_BF16, TINFER_INT4 = 0, 1
 TINFER_SCALE_FP16, TINFER_SCALE_BF16 = 0, 1
 TINFER_MEGAKERNEL, TINFER_GRAPH = 0, 1
 TINFER_Q_GRID, TINFER_Q_SMEM, TINFER_Q_RING_STAGES, TINFER_Q_SLOT_BYTES, TINFER_Q_KERNELS_PER_STEP, \
-    TINFER_Q_TRACE_BYTES = range(6)
+    TINFER_Q_TRACE_BYTES, TINFER_Q_BLOCK_THREADS = range(7)
 TINFER_EPI_STORE, TINFER_EPI_RESIDUAL, TINFER_EPI_SWIGLU, TINFER_EPI_ARGMAX = range(4)
 TINFER_NOALLOC_SCRATCH_BYTES = 1 << 20
 

@@ -576,6 +576,7 @@ long long tinfer_query(const tinfer_ctx* x, int what) {
   if (!x) return -1;
   switch (what) {
     case TINFER_Q_GRID: return x->p.grid;
+    case TINFER_Q_BLOCK_THREADS: return x->cfg.exec_mode == TINFER_MEGAKERNEL ? NTHREADS_MEGA : NTHREADS;
     case TINFER_Q_SMEM: return (long long)x->smem_mega;
     case TINFER_Q_RING_STAGES: return x->stages_mega;
     case TINFER_Q_SLOT_BYTES: return x->slot;

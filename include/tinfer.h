@@ -137,9 +137,10 @@ tinfer_status tinfer_get_error(tinfer_ctx* ctx);
 
 /* Introspection: TINFER_Q_GRID (CTAs of the persistent launch = SM count), TINFER_Q_SMEM (dynamic
  * shared memory per CTA of the persistent kernel), TINFER_Q_RING_STAGES, TINFER_Q_SLOT_BYTES,
- * TINFER_Q_KERNELS_PER_STEP (kernel launches one step makes). Returns -1 for an unknown query. */
+ * TINFER_Q_KERNELS_PER_STEP (kernel launches one step makes), TINFER_Q_BLOCK_THREADS (threads per
+ * CTA of the step kernels of the context's mode). Returns -1 for an unknown query. */
 enum { TINFER_Q_GRID = 0, TINFER_Q_SMEM = 1, TINFER_Q_RING_STAGES = 2, TINFER_Q_SLOT_BYTES = 3,
-       TINFER_Q_KERNELS_PER_STEP = 4, TINFER_Q_TRACE_BYTES = 5 };
+       TINFER_Q_KERNELS_PER_STEP = 4, TINFER_Q_TRACE_BYTES = 5, TINFER_Q_BLOCK_THREADS = 6 };
 long long tinfer_query(const tinfer_ctx* ctx, int what);
 
 /* Per-worker timeline of the persistent kernel ("Decoding in tiles", section 5, Figure 9: each
