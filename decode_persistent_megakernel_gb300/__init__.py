@@ -21,6 +21,7 @@ TINFER_Q_GRID, TINFER_Q_SMEM, TINFER_Q_RING_STAGES, TINFER_Q_SLOT_BYTES, TINFER_
     TINFER_Q_TRACE_BYTES, TINFER_Q_BLOCK_THREADS = range(7)
 TINFER_EPI_STORE, TINFER_EPI_RESIDUAL, TINFER_EPI_SWIGLU, TINFER_EPI_ARGMAX = range(4)
 TINFER_NOALLOC_SCRATCH_BYTES = 1 << 20
+TRACE_FIELDS = 10  # stamps per CTA and phase of the timeline (tinfer_set_trace)
 
 EXPORTS = [
     "tinfer_status_string", "tinfer_check_config", "tinfer_packed_layer_bytes", "tinfer_pack_layer",
@@ -322,8 +323,8 @@ class Engine:
         _check(rc, "tinfer_decode_step_dev")
 
     def trace_step(self, token: int, pos: int):
-        """Runs one traced megakernel step; returns int64 stamps [grid][phases][8] (ns, relative to
-        the earliest stamp)."""
+        """Runs one traced megakernel step; returns int64 stamps [grid][phases][fields] (ns,
+        relative to the earliest stamp; 0 stays 0 where nothing was recorded)."""
         import numpy as np
         import torch
         nbytes = self.query(TINFER_Q_TRACE_BYTES)
@@ -332,8 +333,8 @@ class Engine:
         self.step(token, pos)
         torch.cuda.synchronize()
         _check(tinfer_set_trace(self.ctx, None), "tinfer_set_trace")
-        t = buf.cpu().numpy().reshape(self.query(TINFER_Q_GRID), -1, 8)
-        return t - t[t > 0].min()
+        t = buf.cpu().numpy().reshape(self.query(TINFER_Q_GRID), -1, TRACE_FIELDS)
+        return np.where(t > 0, t - t[t > 0].min(), 0)
 
     def error(self) -> int:
         return tinfer_get_error(self.ctx)

@@ -50,19 +50,15 @@ int max_row_bytes(const tinfer_config* c) {
 
 // bytes of the shared-memory copy of the widest GEMV input vector (fp32 hidden, attention output or
 // SwiGLU output)
-int xs_bytes_for(const tinfer_config* c) {
-  int n = c->hidden;
-  if (c->n_heads * c->head_dim > n) n = c->n_heads * c->head_dim;
-  if (c->ffn > n) n = c->ffn;
-  return (int)align_up((size_t)n * 4, 128);
-}
+
 
 int slot_bytes_for(const tinfer_config* c) {
   const int m = max_row_bytes(c);
   return m <= SLOT_MIN ? SLOT_MIN : (int)align_up((size_t)m, 1024);
 }
 
-// Chunks per KV head the attention may use at any position (the partial buffers' capacity).
+// Chunks per KV head the attention uses at any position up to max_ctx (the partial buffers'
+// capacity), by the device split's rule: enough chunks to cover the grid, each fitting one slot.
 int nch_capacity(int max_ctx, int nkv, int d, int grid, int slot) {
   int tmax = slot / (2 * d);
   if (tmax > T_MAX) tmax = T_MAX;
@@ -71,6 +67,14 @@ int nch_capacity(int max_ctx, int nkv, int d, int grid, int slot) {
   if (want < 1) want = 1;
   if (want > T_MAX) want = T_MAX;
   return nmin > want ? nmin : want;
+}
+
+// The input-vector buffer: the longest GEMV input in fp32.
+int xs_bytes_for(const tinfer_config* c) {
+  int n = c->hidden;
+  if (c->n_heads * c->head_dim > n) n = c->n_heads * c->head_dim;
+  if (c->ffn > n) n = c->ffn;
+  return (int)align_up((size_t)n * 4, 128);
 }
 
 void rope_table(std::vector<float2>& t, int max_ctx, int d, double theta) {
@@ -160,7 +164,6 @@ tinfer_status tinfer_check_config(const tinfer_config* c) {
     return TINFER_ERR_INVALID_ARG;
   if (c->hidden % 8 != 0 || !seg_ok(TINFER_BF16, c->hidden)) return TINFER_ERR_UNSUPPORTED;  // LM head
   if (model_nchl(c) == 0) return TINFER_ERR_UNSUPPORTED;
-  if ((size_t)c->hidden * 4 > (size_t)slot_bytes_for(c)) return TINFER_ERR_UNSUPPORTED;  // gain stage
   const int slot = slot_bytes_for(c);
   int tmax = slot / (2 * c->head_dim);
   if (tmax > T_MAX) tmax = T_MAX;
@@ -662,7 +665,7 @@ tinfer_status tinfer_op_gemv(int fmt, int group, int scale_dtype, int rows, int 
   if (gain_dev && (reinterpret_cast<uintptr_t>(gain_dev) & 15) != 0) return TINFER_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(packed_dev) & 15) != 0) return TINFER_ERR_INVALID_ARG;
   TRY(op_scratch());
-  size_t need_slot = std::max(rb * 2, gain_dev ? (size_t)cols * 4 : (size_t)0);
+  size_t need_slot = rb * 2;
   const int slot = need_slot <= SLOT_MIN ? SLOT_MIN : (int)align_up(need_slot, 1024);
   const int stages = 4;
   const int xs = (int)align_up((size_t)cols * 4, 128);

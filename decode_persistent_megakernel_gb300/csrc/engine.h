@@ -120,7 +120,9 @@ enum TraceField : int {
   TR_ACT = 5,        // the phase's input activations are in registers (before the norm)
   TR_ENTRY = 6,      // the GEMV code of the phase starts (after the phase set-up)
   TR_FETCHED = 7,    // the input vector is in shared memory
-  TRACE_FIELDS = 8
+  TR_AUX0 = 8,       // attention: the first unit's values have arrived (softmax done)
+  TR_AUX1 = 9,       // attention: this CTA won a merge ticket and starts merging
+  TRACE_FIELDS = 10
 };
 
 // Op-level GEMV description (the single-operation entry point uses the same device code).

@@ -40,7 +40,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) op_gemv_kernel(const __grid_const
   if (tid >= NCT) {
     if (tid == NCT) {
       bool dead = false;
-      produce_rows(pp, g, rs, policy_evict_first(), dead, q.gain, q.gain ? (uint32_t)q.cols * 4u : 0u);
+      produce_rows(pp, g, rs, policy_evict_first(), dead);
       prod_drain(pp);
     }
   } else {

@@ -74,12 +74,7 @@ __device__ __forceinline__ void produce_phase(const StepParams& p, Pipe& pp, int
     return;
   }
   const GemvDesc g = phase_gemv(p, phase, layer);
-  const void* gain = nullptr;
-  uint32_t gain_bytes = 0;
-  if (phase == PH_QKV) { gain = p.layers[layer].g1; gain_bytes = p.m.H * 4; }
-  else if (phase == PH_GU) { gain = p.layers[layer].g2; gain_bytes = p.m.H * 4; }
-  else if (phase == PH_LM) { gain = p.final_norm; gain_bytes = p.m.H * 2; }
-  produce_rows(pp, g, row_split(g, blockIdx.x, p.grid, p.slot_bytes), pol_w, dead, gain, gain_bytes);
+  produce_rows(pp, g, row_split(g, blockIdx.x, p.grid, p.slot_bytes), pol_w, dead);
 }
 
 // Timeline slot of (this CTA, phase k, field); null when the launch records no timeline. The
@@ -93,15 +88,13 @@ __device__ __forceinline__ unsigned long long* trace_at(unsigned long long* trac
 }
 
 // The persistent producer's view of the step: one pass over this CTA's copy schedule, stage by
-// stage, in the order the consumers take them (per GEMV phase the gain vector if the phase
-// normalises, then its rows; per attention unit the cached K chunk, then the V chunk).
+// stage, in the order the consumers take them (per GEMV phase its rows; per attention unit the
+// cached K chunk, then the V chunk).
 struct StageCursor {
-  int k, j;                        // phase index, stage within the phase (-1: gain stage)
+  int k, j;                        // phase index, stage within the phase
   int attn;                        // the phase is attention
   const uint8_t* w;                // GEMV: matrix, row bytes, this CTA's rows, rows per stage
   int rb, r0, r1, nr;
-  const void* gain;
-  int gain_bytes;
   const uint16_t* kc;              // attention: this layer's K and V caches
   const uint16_t* vc;
   int u, units, nch, cl, sub;      // unit cursor, split, K/V half of the unit
@@ -122,11 +115,7 @@ static __device__ void cursor_enter(const StepParams& p, StageCursor& c, int pos
   const GemvDesc g = phase_gemv(p, phase, layer);
   const RowSplit rs = row_split(g, blockIdx.x, p.grid, p.slot_bytes);
   c.attn = 0; c.w = g.w; c.rb = g.rb; c.r0 = rs.r0; c.r1 = rs.r1; c.nr = rs.nr;
-  c.gain = nullptr; c.gain_bytes = 0;
-  if (phase == PH_QKV) { c.gain = p.layers[layer].g1; c.gain_bytes = p.m.H * 4; }
-  else if (phase == PH_GU) { c.gain = p.layers[layer].g2; c.gain_bytes = p.m.H * 4; }
-  else if (phase == PH_LM) { c.gain = p.final_norm; c.gain_bytes = p.m.H * 2; }
-  c.j = c.gain ? -1 : 0;
+  c.j = 0;
 }
 
 static __device__ bool cursor_next(const StepParams& p, StageCursor& c, int pos, const void*& src,
@@ -134,7 +123,6 @@ static __device__ bool cursor_next(const StepParams& p, StageCursor& c, int pos,
   const int nph = p.m.L * PHASES_PER_LAYER + 1;
   while (c.k < nph) {
     if (!c.attn) {
-      if (c.j < 0) { src = c.gain; bytes = (uint32_t)c.gain_bytes; c.j = 0; return true; }
       const int s0 = c.r0 + c.j * c.nr;
       if (s0 < c.r1) {
         src = c.w + (size_t)s0 * c.rb;
@@ -247,7 +235,11 @@ __device__ __forceinline__ Pipe consume_attn_phase(const StepParams& p, Pipe pp,
   const AttnArgs A = step_attn_args(p, layer, pos);
   const AttnSplit sp = attn_split(pos, A.nkv, A.d, p.grid, p.slot_bytes, p.n_chunks_override);
   const int units = A.nkv * sp.nch;
-  for (int u = blockIdx.x; u < units; u += p.grid) attn_unit(pp, A, sp, u / sp.nch, u % sp.nch, tid);
+  unsigned long long* tr = trace_at(trace, p, k, 0);  // the first unit of the CTA records sub-steps
+  for (int u = blockIdx.x; u < units; u += p.grid) {
+    attn_unit(pp, A, sp, u / sp.nch, u % sp.nch, tid, tr);
+    tr = nullptr;
+  }
   return pp;
 }
 

@@ -196,6 +196,19 @@ __device__ __forceinline__ void pipe_setup(Pipe& pp) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 __device__ __forceinline__ float bf16_to_f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+// Typed pointer to the dynamic shared memory at shared address `addr`. Loads through it are plain
+// C++ loads the compiler knows to be shared-memory loads, so it can batch and reorder them (the
+// barrier and mbarrier waits carry memory clobbers, which keep the loads after the waits).
+extern __shared__ __align__(128) unsigned char tinfer_dyn_smem[];
+template <class T>
+__device__ __forceinline__ const T* sptr(uint32_t addr) {
+  return reinterpret_cast<const T*>(tinfer_dyn_smem + (addr - smem_addr(tinfer_dyn_smem)));
+}
+template <class T>
+__device__ __forceinline__ T* sptr_w(uint32_t addr) {
+  return reinterpret_cast<T*>(tinfer_dyn_smem + (addr - smem_addr(tinfer_dyn_smem)));
+}
+
 __device__ __forceinline__ uint16_t f_to_bf16_bits(float v) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
@@ -336,42 +349,103 @@ __device__ __forceinline__ void best_update(Best& b, float v, int i) {
   else if (v > b.v || (v == b.v && i < b.i)) { b.v = v; b.i = i; }
 }
 
+constexpr int FETCH_IF = 4;  // 16-byte blocks a thread has in flight per turn of the vector fetch
+constexpr int GAIN_PRE = 4;  // gain blocks a thread loads ahead (vectors of up to 4 * 4 * NCT inputs)
+
+__device__ __forceinline__ float4 gain_block(const ActSrc& src, int j) {
+  if (src.gf) return __ldg(reinterpret_cast<const float4*>(src.gf) + j);
+  const uint2 w = __ldg(reinterpret_cast<const uint2*>(src.gb) + j);
+  return make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+}
+
 // The phase's input vector, written by other CTAs before the last grid barrier, fetched once per
-// CTA into shared memory by all consumer threads together (16-byte loads through L2, batched four
-// deep): every warp of every CTA reading the same few cache lines serialises on those lines, one
-// read per CTA does not, and the load path does not queue behind the CTA's own bulk weight copies.
-// Called by all consumer threads; returns after the named barrier that publishes the copy.
-__device__ __forceinline__ void fetch_vector(Pipe& pp, const void* src, uint32_t bytes, int tid) {
-  const uint4* g = reinterpret_cast<const uint4*>(src);
-  const int n16 = (int)(bytes / 16u);
-  for (int i0 = tid; i0 < n16; i0 += 4 * NCT) {
-    uint4 v[4];
+// CTA into shared memory by all consumer threads together (16-byte loads through L2, thread t
+// taking blocks t, t + NCT, ...): every warp of every CTA reading the same few cache lines
+// serialises on those lines, one read per CTA does not, and the load path does not queue behind
+// the CTA's own bulk weight copies. With an RMSNorm gain the stored values are x * g (the first
+// GAIN_PRE gain blocks of the thread come from `gpre`, loaded before the barrier) and the sum of
+// squares of x is reduced on the way; the return value is 1 / rms(x) (1 without a norm), the same in
+// every consumer thread. Returns after the named barrier that publishes the copy.
+__device__ __forceinline__ float fetch_vector(Pipe& pp, const ActSrc& src, const float4* gpre, int tid) {
+  const bool norm = src.gf || src.gb;
+  const int nb = src.n / 4;
+  float4* xs = sptr_w<float4>(pp.xs);
+  float ss = 0.f;
+  for (int j0 = tid, turn = 0; j0 < nb; j0 += FETCH_IF * NCT, ++turn) {
+    float4 x[FETCH_IF];
+    if (src.xf) {
+      const float4* xf = reinterpret_cast<const float4*>(src.xf);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = i0 + u * NCT;
-      if (i < n16) v[u] = __ldcg(g + i);
+      for (int u = 0; u < FETCH_IF; ++u) {
+        const int j = j0 + u * NCT;
+        x[u] = j < nb ? __ldcg(xf + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    } else {
+      const uint2* xb = reinterpret_cast<const uint2*>(src.xb);
+#pragma unroll
+      for (int u = 0; u < FETCH_IF; ++u) {
+        const int j = j0 + u * NCT;
+        const uint2 w = j < nb ? __ldg(xb + j) : make_uint2(0u, 0u);
+        x[u] = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+      }
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = i0 + u * NCT;
-      if (i < n16)
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(pp.xs + (uint32_t)i * 16u),
-                     "r"(v[u].x), "r"(v[u].y), "r"(v[u].z), "r"(v[u].w)
-                     : "memory");
+    for (int u = 0; u < FETCH_IF; ++u) {
+      const int j = j0 + u * NCT;
+      if (j < nb) {
+        ss = fmaf(x[u].x, x[u].x, ss);
+        ss = fmaf(x[u].y, x[u].y, ss);
+        ss = fmaf(x[u].z, x[u].z, ss);
+        ss = fmaf(x[u].w, x[u].w, ss);
+        float4 g = make_float4(1.f, 1.f, 1.f, 1.f);
+        if (norm) g = (gpre && turn == 0) ? gpre[u] : gain_block(src, j);
+        xs[j] = make_float4(x[u].x * g.x, x[u].y * g.y, x[u].z * g.z, x[u].w * g.w);
+      }
     }
   }
+  if (norm) {
+    ss = warp_sum(ss);
+    if ((tid & 31) == 0) pp.ms->wred[tid >> 5] = ss;
+  }
   named_sync(BAR_CONS, NCT);
+  if (!norm) return 1.f;
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < NCW; ++w) tot += pp.ms->wred[w];
+  return 1.f / sqrtf(tot / (float)src.n + src.eps);
 }
-// 8 consecutive activations from the shared-memory vector (fp32 or bf16 source), index i % 8 == 0
-__device__ __forceinline__ void vec8(const Pipe& pp, bool f32, int i, float* o) {
-  if (f32) {
-    const uint4 u = lds128(pp.xs + (uint32_t)i * 4u), w = lds128(pp.xs + (uint32_t)i * 4u + 16u);
-    o[0] = __uint_as_float(u.x); o[1] = __uint_as_float(u.y); o[2] = __uint_as_float(u.z); o[3] = __uint_as_float(u.w);
-    o[4] = __uint_as_float(w.x); o[5] = __uint_as_float(w.y); o[6] = __uint_as_float(w.z); o[7] = __uint_as_float(w.w);
+
+// One lane's chunk of the input vector from the shared-memory copy: E / 4 consecutive 16-byte blocks
+// starting at block `blk0`. Lanes of a warp own chunks 32 or 128 bytes apart, so the blocks are
+// visited in a lane-rotated order (rotation lane % R, R = E / 4 for int4, 2 for bf16 with the
+// rotation switching at lane 4) that spreads a quarter-warp's loads over all banks; the blocks are
+// then rotated back into place in registers.
+template <int E>
+__device__ __forceinline__ void load_chunk(const float4* xs, int blk0, int lane, float4 (&v)[E / 4]) {
+  constexpr int B = E / 4;
+  if (B == 2) {
+    const int h = (lane >> 2) & 1;
+    const float4 p = xs[blk0 + h], q = xs[blk0 + (h ^ 1)];
+    v[0] = h ? q : p;
+    v[B - 1] = h ? p : q;
   } else {
-    const uint4 b = lds128(pp.xs + (uint32_t)i * 2u);
-    o[0] = bf16_lo(b.x); o[1] = bf16_hi(b.x); o[2] = bf16_lo(b.y); o[3] = bf16_hi(b.y);
-    o[4] = bf16_lo(b.z); o[5] = bf16_hi(b.z); o[6] = bf16_lo(b.w); o[7] = bf16_hi(b.w);
+    const int r = lane & (B - 1);
+    float4 t[B];
+#pragma unroll
+    for (int b = 0; b < B; ++b) t[b] = xs[blk0 + ((b + r) & (B - 1))];
+    // t[b] holds block (b + r) mod B: rotate right by r to put block b at v[b]
+#pragma unroll
+    for (int sh = 1; sh < B; sh <<= 1) {
+      if (r & sh) {
+        float4 u[B];
+#pragma unroll
+        for (int b = 0; b < B; ++b) u[b] = t[(b - sh + B) & (B - 1)];
+#pragma unroll
+        for (int b = 0; b < B; ++b) t[b] = u[b];
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < B; ++b) v[b] = t[b];
   }
 }
 
@@ -385,8 +459,8 @@ __device__ __forceinline__ void vec8(const Pipe& pp, bool f32, int i, float* o) 
 // per-segment row results in shared memory, and one pass at the end of the phase sums the
 // segments in a fixed order and applies the epilogue (bias, residual add, SwiGLU on gate/up pairs).
 // Everything a GEMV phase needs that does not depend on other CTAs' results of the previous phase.
-// The persistent kernel builds it before the grid barrier, so that its cost (descriptors, the row
-// split, cold code, the residual or bias operand and the wait for the gain stage) hides under the
+// The persistent kernel builds it between its arrival at the grid barrier and its wait, so that
+// its cost (descriptors, the row split, cold code, the residual or bias operand) hides under the
 // barrier wait instead of adding to the phase.
 struct GemvPlan {
   GemvDesc g;
@@ -394,11 +468,12 @@ struct GemvPlan {
   ActSrc src;
   Epi epi;
   float pre;     // epilogue operand of row rs.r0 + tid (residual x or bias), fetched early
-  uint32_t gs;   // shared address of the phase's gain stage (RMSNorm phases), already acquired
+  float4 gpre[GAIN_PRE];  // RMSNorm gain blocks tid + u * NCT this thread multiplies in
 };
 
 // Completes a plan whose g, rs, src and epi are set: loads the early epilogue operand (the residual
-// rows are this CTA's own from its previous write, or the constant bias) and acquires the gain stage.
+// rows are this CTA's own from its previous write, or the constant bias) and the thread's RMSNorm
+// gain blocks (constants: their first touch may miss to HBM, which the barrier wait then hides).
 __device__ __forceinline__ void gemv_plan_finish(Pipe& pp, GemvPlan& pl, int tid) {
   const SegInfo si = seg_info(pl.g.fmt, pl.g.cols);
   const int nrows = pl.rs.r1 - pl.rs.r0;
@@ -408,7 +483,15 @@ __device__ __forceinline__ void gemv_plan_finish(Pipe& pp, GemvPlan& pl, int tid
     if (pl.epi.kind == EK_RESIDUAL) pl.pre = __ldcg(pl.epi.y + pl.rs.r0 + tid);
     else if (pl.epi.kind == EK_STORE && pl.epi.bias) pl.pre = __ldg(pl.epi.bias + pl.rs.r0 + tid);
   }
-  pl.gs = (pl.src.gf || pl.src.gb) ? cons_acquire(pp) : 0u;
+  (void)pp;
+  if (pl.src.gf || pl.src.gb) {
+    const int nb = pl.src.n / 4;
+#pragma unroll
+    for (int u = 0; u < GAIN_PRE; ++u) {
+      const int j = tid + u * NCT;
+      pl.gpre[u] = j < nb ? gain_block(pl.src, j) : make_float4(1.f, 1.f, 1.f, 1.f);
+    }
+  }
 }
 
 template <int FMT, int NCHL>
@@ -429,70 +512,33 @@ __device__ void gemv_rows(Pipe& pp, const GemvPlan& pl, Best& best, int tid,
   const bool norm = src.gf || src.gb;
   const float pre = pl.pre;
 
-  // activations of this warp's segment from the shared-memory copy of the input vector; chunks
-  // past the segment read the last valid chunk and are zeroed, so that the row loop needs no
-  // per-lane branches
+  // the input vector (x * g for RMSNorm phases) into shared memory, then this warp's segment into
+  // registers, scaled by 1 / rms(x); chunks past the segment read the segment's last chunk slot and
+  // are zeroed, so that the row loop needs no per-lane branches
   if (tr_ready && tid == 0) tr_ready[TR_ENTRY - TR_READY] = globaltimer();
-  fetch_vector(pp, src.xf ? (const void*)src.xf : (const void*)src.xb,
-               (uint32_t)src.n * (src.xf ? 4u : 2u), tid);
+  const float inv = fetch_vector(pp, src, pl.gpre, tid);
   if (tr_ready && tid == 0) tr_ready[TR_FETCHED - TR_READY] = globaltimer();
+  (void)norm;
   float a[NCHL][E];
   float S[NCHL];
-  float ss = 0.f;
-#pragma unroll
-  for (int k = 0; k < NCHL; ++k) {
-    const int c = min(lane + 32 * k, si.chs - 1);
-    const int base = seg * si.ks + c * E;
-    const bool ok = lane + 32 * k < si.chs;
-#pragma unroll
-    for (int e = 0; e < E; e += 8) {
-      vec8(pp, src.xf != nullptr, base + e, &a[k][e]);  // clamped chunk: always a valid address
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        a[k][e + u] = ok ? a[k][e + u] : 0.f;
-        ss = fmaf(a[k][e + u], a[k][e + u], ss);
-      }
-    }
-  }
-  if (tr_ready && tid == 0) tr_ready[TR_ACT - TR_READY] = globaltimer() + (unsigned long long)(ss * 0.f);
-  if (norm) {
-    float tot = warp_sum(ss);
-    if (si.nseg > 1) {
-      if (grp == 0 && lane == 0) ms->wred[seg] = tot;
-      named_sync(BAR_CONS, NCT);
-      tot = 0.f;
-      for (int s2 = 0; s2 < si.nseg; ++s2) tot += ms->wred[s2];
-    }
-    const float inv = 1.f / sqrtf(tot / (float)src.n + src.eps);
-    // the gain vector is the phase's first ring stage (fp32, or bf16 for the final norm)
-    const uint32_t gs = pl.gs;
+  {
+    const float4* xsv = sptr<float4>(pp.xs);
 #pragma unroll
     for (int k = 0; k < NCHL; ++k) {
-      {
-        const int c = min(lane + 32 * k, si.chs - 1);
-        const int base = seg * si.ks + c * E;
+      const bool ok = lane + 32 * k < si.chs;
+      const int c = min(lane + 32 * k, si.chs - 1);  // clamped chunk: always a valid address
+      float4 v[E / 4];
+      load_chunk<E>(xsv, (seg * si.ks + c * E) / 4, lane, v);
 #pragma unroll
-        for (int e = 0; e < E; e += 8) {
-          float gv[8];
-          if (src.gf) {
-            const uint4 g0 = lds128(gs + (uint32_t)(base + e) * 4u);
-            const uint4 g1 = lds128(gs + (uint32_t)(base + e) * 4u + 16u);
-            gv[0] = __uint_as_float(g0.x); gv[1] = __uint_as_float(g0.y);
-            gv[2] = __uint_as_float(g0.z); gv[3] = __uint_as_float(g0.w);
-            gv[4] = __uint_as_float(g1.x); gv[5] = __uint_as_float(g1.y);
-            gv[6] = __uint_as_float(g1.z); gv[7] = __uint_as_float(g1.w);
-          } else {
-            const uint4 gb = lds128(gs + (uint32_t)(base + e) * 2u);
-            gv[0] = bf16_lo(gb.x); gv[1] = bf16_hi(gb.x); gv[2] = bf16_lo(gb.y); gv[3] = bf16_hi(gb.y);
-            gv[4] = bf16_lo(gb.z); gv[5] = bf16_hi(gb.z); gv[6] = bf16_lo(gb.w); gv[7] = bf16_hi(gb.w);
-          }
-#pragma unroll
-          for (int u = 0; u < 8; ++u) a[k][e + u] = a[k][e + u] * inv * gv[u];
-        }
+      for (int b = 0; b < E / 4; ++b) {
+        a[k][4 * b + 0] = ok ? v[b].x * inv : 0.f;
+        a[k][4 * b + 1] = ok ? v[b].y * inv : 0.f;
+        a[k][4 * b + 2] = ok ? v[b].z * inv : 0.f;
+        a[k][4 * b + 3] = ok ? v[b].w * inv : 0.f;
       }
     }
-    cons_release(pp, lane);
   }
+  if (tr_ready && tid == 0) tr_ready[TR_ACT - TR_READY] = globaltimer() + (unsigned long long)(a[0][0] * 0.f);
   if (FMT == 1) {
 #pragma unroll
     for (int k = 0; k < NCHL; ++k) {
@@ -618,9 +664,7 @@ __device__ __forceinline__ void gemv_consume_any(Pipe& pp, const GemvPlan& pl, B
 }
 
 __device__ __forceinline__ void produce_rows(Pipe& pp, const GemvDesc& g, const RowSplit& rs,
-                                             uint64_t pol, bool& dead, const void* gain = nullptr,
-                                             uint32_t gain_bytes = 0) {
-  if (gain_bytes) prod_push(pp, gain, gain_bytes, pol, dead);
+                                             uint64_t pol, bool& dead) {
   for (int s0 = rs.r0; s0 < rs.r1; s0 += rs.nr) {
     const int nrs = min(rs.nr, rs.r1 - s0);
     prod_push(pp, g.w + (size_t)s0 * g.rb, (uint32_t)(nrs * g.rb), pol, dead);
@@ -697,8 +741,10 @@ struct AttnSplit {
   int cl;   // slots per chunk
 };
 
-// Split of [0, pos] into chunks: enough chunks that KV heads x chunks covers the grid, each chunk
-// no longer than one ring slot holds (and T_MAX); trailing chunks may be empty.
+// Split of [0, pos] into chunks: enough chunks that the units (KV head, chunk) cover the grid, each
+// chunk no longer than min(slot / (2 d), T_MAX) positions (its keys fill at most one ring slot). The
+// unit's work is latency-bound, so spreading it over every SM beats fewer, longer chunks even with
+// the merge's extra partials. override_nch > 0 fixes the count (single-op tests).
 __device__ __forceinline__ AttnSplit attn_split(int pos, int nkv, int d, int grid, int slot,
                                                 int override_nch) {
   const int n_ctx = pos + 1;
@@ -743,52 +789,187 @@ __device__ __forceinline__ void produce_attn_unit(Pipe& pp, const AttnArgs& A, i
   prod_push(pp, A.vc + base, (uint32_t)(nk * A.d * 2), pol, dead);
 }
 
-// Merge of one KV head's chunk partials for its query heads (the log-sum-exp combine). Warp g finds
-// head g's maximum and weights (lanes over chunks), then each output element sums its chunks'
-// unnormalised outputs in a fixed order, eight loads in flight at a time.
+// Merge of one KV head's chunk partials for its query heads (the log-sum-exp combine). Every
+// thread first issues the loads of its output element's chunk outputs (they do not depend on the
+// weights), warp g meanwhile finds head g's maximum and weights (lanes over chunks); then each output
+// sums its chunks in a fixed order.
 static __device__ void attn_merge(const AttnArgs& A, Misc* ms, int tid, int j, int nch) {
+  constexpr int MB = 32;  // chunk outputs in flight per thread
   const int G = A.nq / A.nkv, d = A.d;
   const int warp = tid >> 5, lane = tid & 31;
+  const int nout = G * d;
+  float ob[MB];
+  const float* po0 = nullptr;
+  if (tid < nout) {
+    const int g = tid / d, i = tid - g * d;
+    po0 = A.part_o + (size_t)(j * G + g) * A.nch_cap * d + i;
+#pragma unroll
+    for (int u = 0; u < MB; ++u) ob[u] = u < nch ? __ldcg(po0 + (size_t)u * d) : 0.f;
+  }
   if (warp < G) {
+    // head g = warp: lanes over chunks, m and l loaded once (up to 8 chunks per lane)
     const int h = j * G + warp;
+    float mc[T_MAX / 32], lc[T_MAX / 32];
     float M = -CUDART_INF_F;
-    for (int c = lane; c < nch; c += 32) M = fmaxf(M, __ldcg(A.part_m + (size_t)h * A.nch_cap + c));
+#pragma unroll
+    for (int k = 0; k < T_MAX / 32; ++k) {
+      const int c = lane + 32 * k;
+      mc[k] = c < nch ? __ldcg(A.part_m + (size_t)h * A.nch_cap + c) : -CUDART_INF_F;
+      lc[k] = c < nch ? __ldcg(A.part_l + (size_t)h * A.nch_cap + c) : 0.f;
+      M = fmaxf(M, mc[k]);
+    }
     M = warp_max(M);
     float den = 0.f;
-    for (int c = lane; c < nch; c += 32) {
-      const float mc = __ldcg(A.part_m + (size_t)h * A.nch_cap + c);
-      const float w = mc == -CUDART_INF_F ? 0.f : expf(mc - M);  // an empty chunk weighs exactly 0
-      ms->sc[warp * T_MAX + c] = w;
-      den = fmaf(w, __ldcg(A.part_l + (size_t)h * A.nch_cap + c), den);
+#pragma unroll
+    for (int k = 0; k < T_MAX / 32; ++k) {
+      const int c = lane + 32 * k;
+      const float w = mc[k] == -CUDART_INF_F ? 0.f : expf(mc[k] - M);  // an empty chunk weighs exactly 0
+      if (c < nch) ms->sc[warp * T_MAX + c] = w;
+      den = fmaf(w, lc[k], den);
     }
     den = warp_sum(den);
     if (lane == 0) ms->hl[warp] = 1.f / den;
   }
   named_sync(BAR_CONS, NCT);
-  for (int idx = tid; idx < G * d; idx += NCT) {
+  for (int idx = tid; idx < nout; idx += NCT) {
     const int g = idx / d, i = idx - g * d;
-    const int h = j * G + g;
-    const float* po = A.part_o + (size_t)h * A.nch_cap * d + i;
+    const float* po = A.part_o + (size_t)(j * G + g) * A.nch_cap * d + i;
+    const float* wg = ms->sc + g * T_MAX;
     float acc = 0.f;
     int c = 0;
-    for (; c + 8 <= nch; c += 8) {
-      float o[8];
+    if (idx == tid) {  // the first batch is already loaded
 #pragma unroll
-      for (int u = 0; u < 8; ++u) o[u] = __ldcg(po + (size_t)(c + u) * d);
-#pragma unroll
-      for (int u = 0; u < 8; ++u) acc = fmaf(ms->sc[g * T_MAX + c + u], o[u], acc);
+      for (int u = 0; u < MB; ++u) acc = u < nch ? fmaf(wg[u], ob[u], acc) : acc;
+      c = MB;
     }
-    for (; c < nch; ++c) acc = fmaf(ms->sc[g * T_MAX + c], __ldcg(po + (size_t)c * d), acc);
-    A.out[(size_t)h * d + i] = acc * ms->hl[g];
+    for (; c < nch; c += MB) {
+#pragma unroll
+      for (int u = 0; u < MB; ++u) ob[u] = c + u < nch ? __ldcg(po + (size_t)(c + u) * d) : 0.f;
+#pragma unroll
+      for (int u = 0; u < MB; ++u) acc = c + u < nch ? fmaf(wg[c + u], ob[u], acc) : acc;
+    }
+    A.out[(size_t)(j * G + g) * d + i] = acc * ms->hl[g];
+  }
+}
+
+// Scores of the cached positions [0, nk) and, when T > nk, of the new position (from kn), for heads
+// g < G into sc[g][t]. Lane groups of LG = d / 8 lanes take one position each: lane li holds dims
+// [8 li, 8 li + 8) of GP >= G query heads in registers and loads one 16-byte key chunk (a warp reads
+// 32 / LG consecutive rows: no bank conflicts). The GP partial sums then meet by a reduce-scatter
+// over the group (each level halves the values a lane keeps), which leaves head li / (LG / GP) in
+// lane li after log2(GP) + log2(LG / GP) shuffles per position instead of GP * log2(LG).
+template <int GP, int LG>
+__device__ __forceinline__ void attn_scores_groups(uint32_t kst, const float* qs, const float* kn,
+                                                   float* sc, int nk, int T, int G, int tid) {
+  static_assert(GP <= LG, "a lane keeps at least one head");
+  constexpr int D = LG * 8, PW = 32 / LG, NW = NCT / 32;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int li = lane % LG, pl = lane / LG;
+  float qr[GP][8];
+#pragma unroll
+  for (int g = 0; g < GP; ++g) {
+    const float4 a = *reinterpret_cast<const float4*>(qs + g * D + li * 8);
+    const float4 b = *reinterpret_cast<const float4*>(qs + g * D + li * 8 + 4);
+    const bool on = g < G;
+    qr[g][0] = on ? a.x : 0.f; qr[g][1] = on ? a.y : 0.f; qr[g][2] = on ? a.z : 0.f; qr[g][3] = on ? a.w : 0.f;
+    qr[g][4] = on ? b.x : 0.f; qr[g][5] = on ? b.y : 0.f; qr[g][6] = on ? b.z : 0.f; qr[g][7] = on ? b.w : 0.f;
+  }
+  const uint4* Ks = sptr<uint4>(kst);
+  for (int tb = warp * PW; tb < T; tb += NW * PW) {
+    const int t = tb + pl;
+    float k8[8];
+    if (t < nk) {
+      const uint4 kv = Ks[(size_t)t * LG + li];
+      k8[0] = bf16_lo(kv.x); k8[1] = bf16_hi(kv.x); k8[2] = bf16_lo(kv.y); k8[3] = bf16_hi(kv.y);
+      k8[4] = bf16_lo(kv.z); k8[5] = bf16_hi(kv.z); k8[6] = bf16_lo(kv.w); k8[7] = bf16_hi(kv.w);
+    } else {  // the new position (t == nk) or past the chunk (t >= T: result unused)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) k8[e] = t < T ? kn[li * 8 + e] : 0.f;
+    }
+    float v[GP];
+#pragma unroll
+    for (int g = 0; g < GP; ++g) {
+      float a = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) a = fmaf(qr[g][e], k8[e], a);
+      v[g] = a;
+    }
+    // reduce-scatter over the LG lanes of the group
+#pragma unroll
+    for (int n = GP, off = LG / 2; off > 0; off >>= 1) {
+      const bool up = (li & off) != 0;
+      if (n > 1) {
+#pragma unroll
+        for (int i = 0; i < GP / 2; ++i) {
+          if (i < n / 2) {
+            const float send = up ? v[i] : v[i + n / 2];
+            const float keep = up ? v[i + n / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+          }
+        }
+        n /= 2;
+      } else {
+        v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+      }
+    }
+    const int head = li / (LG / GP);
+    if (li % (LG / GP) == 0 && head < G && t < T) sc[head * T_MAX + t] = v[0];
+  }
+}
+
+// The same scores, one thread per (head, position) with a full dot product (any d multiple of 8);
+// key chunks in a rotated order so that the lanes of a quarter-warp hit distinct banks.
+__device__ __forceinline__ void attn_scores_threads(uint32_t kst, const float* qs, const float* kn,
+                                                    float* sc, int nk, int T, int G, int d, int tid) {
+  const uint4* Ks = sptr<uint4>(kst);
+  const int nc = d / 8;
+  for (int idx = tid; idx < G * T; idx += NCT) {
+    const int g = idx / T, t = idx - g * T;
+    const float* qg = qs + g * d;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    if (t < nk) {
+      const uint4* krow = Ks + (size_t)t * nc;
+      int ch = t % nc;
+      for (int cc = 0; cc < nc; ++cc) {
+        const uint4 kv = krow[ch];
+        const float4 qa = *reinterpret_cast<const float4*>(qg + ch * 8);
+        const float4 qb = *reinterpret_cast<const float4*>(qg + ch * 8 + 4);
+        a0 = fmaf(qa.x, bf16_lo(kv.x), a0);
+        a1 = fmaf(qa.y, bf16_hi(kv.x), a1);
+        a2 = fmaf(qa.z, bf16_lo(kv.y), a2);
+        a3 = fmaf(qa.w, bf16_hi(kv.y), a3);
+        a0 = fmaf(qb.x, bf16_lo(kv.z), a0);
+        a1 = fmaf(qb.y, bf16_hi(kv.z), a1);
+        a2 = fmaf(qb.z, bf16_lo(kv.w), a2);
+        a3 = fmaf(qb.w, bf16_hi(kv.w), a3);
+        ch = ch + 1 == nc ? 0 : ch + 1;
+      }
+    } else {
+      for (int i = 0; i < d; i += 4) {
+        a0 = fmaf(qg[i], kn[i], a0);
+        a1 = fmaf(qg[i + 1], kn[i + 1], a1);
+        a2 = fmaf(qg[i + 2], kn[i + 2], a2);
+        a3 = fmaf(qg[i + 3], kn[i + 3], a3);
+      }
+    }
+    sc[g * T_MAX + t] = (a0 + a1) + (a2 + a3);
   }
 }
 
 // One attention unit: KV head j, chunk c. RoPE on the group's queries (and, in the chunk holding
 // pos, on the new key, which is written to the cache with the new value), scores over the chunk,
 // per-head max / exponentials / sum, the value sum, and the partial (m, l, o) of the chunk
-// ("One launch per token", "The attention trap"; tinyinfer, "Round 2": one block per KV head and
-// chunk serving all grouped query heads, K/V read once). The last CTA done with head j merges.
-static __device__ void attn_unit(Pipe& pp, const AttnArgs& A, const AttnSplit& sp, int j, int c, int tid) {
+// ("One launch per token", "The attention trap"; "How I built an LLM inference engine", "Round 2":
+// one unit per KV head and chunk serving all grouped query heads, K/V read once). The last CTA done
+// with head j merges. The work is spread so that no step waits on a long dependent chain:
+//   scores: one thread per (head, position), a full dot product over d; the 16-byte key chunks are
+//           visited in a rotated order so that the 8 lanes of a quarter-warp hit distinct banks;
+//   values: one thread per (head, dimension), four independent accumulators over the positions.
+// tr: optional timeline row of the phase (fields TR_READY, TR_ACT, TR_ENTRY, TR_AUX0, TR_FETCHED,
+// TR_AUX1 receive the keys' arrival, the ends of the query set-up and the scores, the values'
+// arrival, the end of the partials and the merge start).
+static __device__ void attn_unit(Pipe& pp, const AttnArgs& A, const AttnSplit& sp, int j, int c, int tid,
+                                 unsigned long long* tr = nullptr) {
   Misc* ms = pp.ms;
   const int lane = tid & 31, warp = tid >> 5;
   const int d = A.d, half = d / 2, G = A.nq / A.nkv;
@@ -796,20 +977,24 @@ static __device__ void attn_unit(Pipe& pp, const AttnArgs& A, const AttnSplit& s
   const int t0 = c * sp.cl;
   const int t1 = min(t0 + sp.cl, n_ctx);
   const bool has_pos = t0 <= pos && pos < t1;
-  const int nk = max(0, min(t1, pos) - t0);
-  const int T = max(0, t1 - t0);
+  const int nk = max(0, min(t1, pos) - t0);  // cached positions, streamed through the ring
+  const int T = max(0, t1 - t0);             // positions of the chunk: nk, plus pos itself
   const float scale = 1.f / sqrtf((float)d);
   const float2* rt = A.rope + (size_t)pos * half;
   const float* q = A.qkv + (size_t)j * G * d;
   const float* kr = A.qkv + (size_t)A.nq * d + (size_t)j * d;
   const float* vr = kr + (size_t)A.nkv * d;
+  float* qs = sptr_w<float>(smem_addr(ms->qs));
+  float* sc = sptr_w<float>(smem_addr(ms->sc));
+  float* kn = sptr_w<float>(smem_addr(ms->kn));
+  float* vn = sptr_w<float>(smem_addr(ms->vn));
 
   for (int idx = tid; idx < G * half; idx += NCT) {
     const int g = idx / half, i = idx - g * half;
     const float x0 = __ldcg(q + g * d + i), x1 = __ldcg(q + g * d + i + half);
     const float2 cs = rt[i];
-    ms->qs[g * d + i] = (x0 * cs.x - x1 * cs.y) * scale;
-    ms->qs[g * d + i + half] = (x1 * cs.x + x0 * cs.y) * scale;
+    qs[g * d + i] = (x0 * cs.x - x1 * cs.y) * scale;
+    qs[g * d + i + half] = (x1 * cs.x + x0 * cs.y) * scale;
   }
   if (has_pos) {
     const size_t slot = ((size_t)j * A.max_ctx + pos) * d;
@@ -820,64 +1005,40 @@ static __device__ void attn_unit(Pipe& pp, const AttnArgs& A, const AttnSplit& s
       const uint16_t b1 = f_to_bf16_bits(x1 * cs.x + x0 * cs.y);
       A.kc[slot + i] = b0;
       A.kc[slot + i + half] = b1;
-      ms->kn[i] = bf16_to_f(b0);
-      ms->kn[i + half] = bf16_to_f(b1);
+      kn[i] = bf16_to_f(b0);
+      kn[i + half] = bf16_to_f(b1);
     }
     for (int i = tid; i < d; i += NCT) {
       const uint16_t b = f_to_bf16_bits(__ldcg(vr + i));
       A.vc[slot + i] = b;
-      ms->vn[i] = bf16_to_f(b);
+      vn[i] = bf16_to_f(b);
     }
   }
   named_sync(BAR_CONS, NCT);
+  if (tr && tid == 0) tr[TR_ACT] = globaltimer();
 
-  // scores: one thread per cached slot; 16-byte chunks of the key row visited in a rotated order
-  // so that the 8 lanes of a quarter-warp hit distinct banks
+  // ---- scores
   const uint32_t kst = cons_acquire(pp);
-  const int nc = d / 8;
-  if (tid < nk) {
-    float s[G_MAX];
-#pragma unroll
-    for (int g = 0; g < G_MAX; ++g) s[g] = 0.f;
-    const uint32_t row = kst + (uint32_t)tid * d * 2;
-    for (int cc = 0; cc < nc; ++cc) {
-      const int ch = (cc + tid) % nc;
-      const uint4 kv = lds128(row + ch * 16);
-      const float k8[8] = {bf16_lo(kv.x), bf16_hi(kv.x), bf16_lo(kv.y), bf16_hi(kv.y),
-                           bf16_lo(kv.z), bf16_hi(kv.z), bf16_lo(kv.w), bf16_hi(kv.w)};
-#pragma unroll
-      for (int g = 0; g < G_MAX; ++g) {
-        if (g < G) {
-          const float* qg = ms->qs + g * d + ch * 8;
-          float t = s[g];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) t = fmaf(qg[e], k8[e], t);
-          s[g] = t;
-        }
-      }
-    }
-#pragma unroll
-    for (int g = 0; g < G_MAX; ++g)
-      if (g < G) ms->sc[g * T_MAX + tid] = s[g];
-  }
-  if (has_pos && tid == nk) {
-    for (int g = 0; g < G; ++g) {
-      float t = 0.f;
-      for (int i = 0; i < d; ++i) t = fmaf(ms->qs[g * d + i], ms->kn[i], t);
-      ms->sc[g * T_MAX + nk] = t;
-    }
-  }
+  if (tr && tid == 0) tr[TR_READY] = globaltimer();  // the chunk's keys have arrived
+  if (d == 64 && G <= 4) attn_scores_groups<4, 8>(kst, qs, kn, sc, nk, T, G, tid);
+  else if (d == 64) attn_scores_groups<8, 8>(kst, qs, kn, sc, nk, T, G, tid);
+  else if (d == 128 && G <= 4) attn_scores_groups<4, 16>(kst, qs, kn, sc, nk, T, G, tid);
+  else if (d == 128) attn_scores_groups<8, 16>(kst, qs, kn, sc, nk, T, G, tid);
+  else attn_scores_threads(kst, qs, kn, sc, nk, T, G, d, tid);
   cons_release(pp, lane);
   named_sync(BAR_CONS, NCT);
+  if (tr && tid == 0) tr[TR_ENTRY] = globaltimer();
 
+  // ---- softmax statistics per head (unnormalised probabilities stay in sc)
   if (warp < G) {
+    float* sg = sc + warp * T_MAX;
     float m = -CUDART_INF_F;
-    for (int t = lane; t < T; t += 32) m = fmaxf(m, ms->sc[warp * T_MAX + t]);
+    for (int t = lane; t < T; t += 32) m = fmaxf(m, sg[t]);
     m = warp_max(m);
     float l = 0.f;
     for (int t = lane; t < T; t += 32) {
-      const float e = expf(ms->sc[warp * T_MAX + t] - m);
-      ms->sc[warp * T_MAX + t] = e;
+      const float e = expf(sg[t] - m);
+      sg[t] = e;
       l += e;
     }
     l = warp_sum(l);
@@ -885,23 +1046,35 @@ static __device__ void attn_unit(Pipe& pp, const AttnArgs& A, const AttnSplit& s
   }
   named_sync(BAR_CONS, NCT);
 
+  // ---- values
   const uint32_t vst = cons_acquire(pp);
-  for (int idx = tid; idx < G * half; idx += NCT) {
-    const int g = idx / half, i2 = idx - g * half;
-    const float* pg = ms->sc + g * T_MAX;
-    float o0 = 0.f, o1 = 0.f;
-    for (int t = 0; t < nk; ++t) {
-      const uint32_t vv = lds32(vst + (uint32_t)(t * d + 2 * i2) * 2u);
-      o0 = fmaf(pg[t], bf16_lo(vv), o0);
-      o1 = fmaf(pg[t], bf16_hi(vv), o1);
+  if (tr && tid == 0) tr[TR_AUX0] = globaltimer();  // the chunk's values have arrived
+  {
+    const uint32_t* Vw = sptr<uint32_t>(vst);  // bf16 pairs, half words per position
+    for (int idx = tid; idx < G * half; idx += NCT) {
+      const int g = idx / half, i2 = idx - g * half;
+      const float* pg = sc + g * T_MAX;
+      const uint32_t* vc = Vw + i2;
+      float2 o0 = make_float2(0.f, 0.f), o1 = o0, o2 = o0, o3 = o0;
+      int t = 0;
+      for (; t + 4 <= nk; t += 4) {
+        const float4 p4 = *reinterpret_cast<const float4*>(pg + t);
+        const uint32_t w0 = vc[(size_t)t * half], w1 = vc[(size_t)(t + 1) * half];
+        const uint32_t w2 = vc[(size_t)(t + 2) * half], w3 = vc[(size_t)(t + 3) * half];
+        o0 = fma2(make_float2(p4.x, p4.x), make_float2(bf16_lo(w0), bf16_hi(w0)), o0);
+        o1 = fma2(make_float2(p4.y, p4.y), make_float2(bf16_lo(w1), bf16_hi(w1)), o1);
+        o2 = fma2(make_float2(p4.z, p4.z), make_float2(bf16_lo(w2), bf16_hi(w2)), o2);
+        o3 = fma2(make_float2(p4.w, p4.w), make_float2(bf16_lo(w3), bf16_hi(w3)), o3);
+      }
+      for (; t < nk; ++t) {
+        const uint32_t w = vc[(size_t)t * half];
+        o0 = fma2(make_float2(pg[t], pg[t]), make_float2(bf16_lo(w), bf16_hi(w)), o0);
+      }
+      if (has_pos) o1 = fma2(make_float2(pg[nk], pg[nk]), make_float2(vn[2 * i2], vn[2 * i2 + 1]), o1);
+      const float2 o = make_float2((o0.x + o1.x) + (o2.x + o3.x), (o0.y + o1.y) + (o2.y + o3.y));
+      const int h = j * G + g;
+      *reinterpret_cast<float2*>(A.part_o + ((size_t)h * A.nch_cap + c) * d + 2 * i2) = o;
     }
-    if (has_pos) {
-      o0 = fmaf(pg[nk], ms->vn[2 * i2], o0);
-      o1 = fmaf(pg[nk], ms->vn[2 * i2 + 1], o1);
-    }
-    const int h = j * G + g;
-    float2* po = reinterpret_cast<float2*>(A.part_o + ((size_t)h * A.nch_cap + c) * d) + i2;
-    *po = make_float2(o0, o1);
   }
   cons_release(pp, lane);
   if (tid < G) {
@@ -910,6 +1083,7 @@ static __device__ void attn_unit(Pipe& pp, const AttnArgs& A, const AttnSplit& s
     A.part_l[(size_t)h * A.nch_cap + c] = ms->hl[tid];
   }
   named_sync(BAR_CONS, NCT);
+  if (tr && tid == 0) tr[TR_FETCHED] = globaltimer();
   if (tid == 0) {
     // release publishes this CTA's partials (ordered before by the barrier); acquire makes the
     // other CTAs' partials visible to the merging CTA
@@ -918,6 +1092,7 @@ static __device__ void attn_unit(Pipe& pp, const AttnArgs& A, const AttnSplit& s
   }
   named_sync(BAR_CONS, NCT);
   if (ms->flag) {
+    if (tr && tid == 0) tr[TR_AUX1] = globaltimer();
     attn_merge(A, ms, tid, j, sp.nch);
     if (tid == 0) atomicExch(A.tickets + j, 0u);
   }

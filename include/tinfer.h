@@ -147,11 +147,12 @@ long long tinfer_query(const tinfer_ctx* ctx, int what);
  * worker's time split into streaming, waiting and small work). When trace_dev is not NULL (device
  * memory of TINFER_Q_TRACE_BYTES bytes, caller-owned), every following megakernel step writes, for
  * every CTA c and phase k (k = 5*layer + {0 QKV, 1 attention, 2 O, 3 gate/up, 4 down}, the LM head
- * last), eight uint64 %globaltimer nanosecond stamps at [(c * phases + k) * 8 + f]: f = 0 phase
- * start (after the previous grid barrier), 1 activations normalised and ready, 2 phase end,
- * 3 producer starts issuing the phase's copies, 4 producer has issued them, 5 input activations in
- * registers, 6 GEMV code entered, 7 input vector in shared memory (5-7: GEMV phases). NULL turns
- * tracing off. */
+ * last), ten uint64 %globaltimer nanosecond stamps at [(c * phases + k) * 10 + f] (0 where nothing
+ * was recorded): f = 0 phase start (after the previous grid barrier), 2 phase end, 3 producer starts
+ * issuing the phase's copies, 4 producer has issued them; GEMV phases: 1 activations normalised and
+ * ready, 5 input activations in registers, 6 GEMV code entered, 7 input vector in shared memory;
+ * attention phases (first unit of the CTA): 1 keys arrived, 5 queries rotated, 6 scores done,
+ * 7 partials written, 8 values arrived, 9 merge started (CTAs that merge). NULL turns tracing off. */
 tinfer_status tinfer_set_trace(tinfer_ctx* ctx, void* trace_dev);
 
 /* Test hooks: timeout of every device-side wait in nanoseconds (default 200 ms), and a fault
