@@ -104,7 +104,7 @@ struct tinfer_ctx {
   int* pinned = nullptr;       // [2] host staging for tinfer_generate
   int* gen_dev = nullptr;      // [2] token in, argmax out for tinfer_generate
   int* argmax_fallback = nullptr;
-  size_t tickets_off = 0, gbar_off = 0, err_off = 0;
+  size_t tickets_off = 0, err_off = 0;
   // graph mode
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t gexec = nullptr;
@@ -325,7 +325,7 @@ tinfer_status tinfer_create(const tinfer_config* c, const tinfer_weights* w, voi
   x->slot = slot_bytes_for(c);
   x->xs_bytes = xs_bytes_for(c);
   const size_t misc = smem_for(0, 0, x->xs_bytes);
-  smem_optin -= 256;  // the persistent kernel's static shared memory
+  smem_optin -= (int)static_smem_mega();  // the persistent kernel's static shared memory
   x->stages_mega = (int)((smem_optin - misc) / x->slot);
   if (x->stages_mega > 8) x->stages_mega = 8;
   while (x->stages_mega > 2 && smem_for(x->stages_mega, x->slot, x->xs_bytes) > (size_t)smem_optin) --x->stages_mega;
@@ -365,17 +365,18 @@ tinfer_status tinfer_create(const tinfer_config* c, const tinfer_weights* w, voi
   // scratch: one allocation
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
-  const size_t o_x = take((size_t)H * 4), o_qkv = take((size_t)qkv_rows * 4);
-  const size_t o_attn = take((size_t)nq * d * 4), o_act = take((size_t)F * 4);
+  // activations handed between phases: stamped 8-byte words
+  const size_t o_xa = take((size_t)H * 8), o_xb = take((size_t)H * 8), o_qkv = take((size_t)qkv_rows * 8);
+  const size_t o_attn = take((size_t)nq * d * 8), o_act = take((size_t)F * 8);
   const size_t o_pm = take((size_t)nq * nch_cap * 4), o_pl = take((size_t)nq * nch_cap * 4);
   const size_t o_po = take((size_t)nq * nch_cap * d * 4);
-  const size_t o_tk = take((size_t)(nkv + 1) * 4), o_gb = take(4);
+  const size_t o_tk = take((size_t)(nkv + 1) * 4);
   const size_t o_bv = take((size_t)grid * 4), o_bi = take((size_t)grid * 4), o_bb = take((size_t)grid * 4);
   const size_t o_err = take(4), o_step = take(2 * 4), o_gen = take(2 * 4), o_am = take(4);
   if ((st = cu(cudaMalloc(&x->scratch, off))) != TINFER_OK) return fail(st);
   if ((st = cu(cudaMemset(x->scratch, 0, off))) != TINFER_OK) return fail(st);
   uint8_t* s = (uint8_t*)x->scratch;
-  x->tickets_off = o_tk; x->gbar_off = o_gb; x->err_off = o_err;
+  x->tickets_off = o_tk; x->err_off = o_err;
 
   // layers
   const LayerLayout LL = layer_layout(H, nq, nkv, d, F, c->weight_format, c->group_size, c->qkv_bias);
@@ -417,10 +418,12 @@ tinfer_status tinfer_create(const tinfer_config* c, const tinfer_weights* w, voi
   p.kcache = (uint16_t*)k_cache_dev;
   p.vcache = (uint16_t*)v_cache_dev;
   p.rope = x->rope_dev;
-  p.x = (float*)(s + o_x); p.qkv = (float*)(s + o_qkv); p.attn = (float*)(s + o_attn);
-  p.act = (float*)(s + o_act);
+  p.xa = (uint64_t*)(s + o_xa); p.xb = (uint64_t*)(s + o_xb); p.qkv = (uint64_t*)(s + o_qkv);
+  p.attn = (uint64_t*)(s + o_attn); p.act = (uint64_t*)(s + o_act);
+  p.epoch = 1;  // the buffers start zeroed: stamp 0 is never expected
+  p.stamp_check = c->exec_mode == TINFER_MEGAKERNEL;
   p.part_m = (float*)(s + o_pm); p.part_l = (float*)(s + o_pl); p.part_o = (float*)(s + o_po);
-  p.tickets = (unsigned*)(s + o_tk); p.gbar = (unsigned*)(s + o_gb);
+  p.tickets = (unsigned*)(s + o_tk);
   p.best_val = (float*)(s + o_bv); p.best_idx = (int*)(s + o_bi); p.best_bad = (int*)(s + o_bb);
   p.err = (int*)(s + o_err);
   p.err_host = x->err_host_dev;
@@ -437,7 +440,6 @@ tinfer_status tinfer_create(const tinfer_config* c, const tinfer_weights* w, voi
     if (const char* e = getenv("TINFER_L2_PACE")) p.l2_pace_ns_per_kb = atoi(e);
     if (const char* e = getenv("TINFER_INFLIGHT")) p.inflight = atoi(e);
   }
-  p.bar_base = 0;
   p.timeout_ns = DEFAULT_TIMEOUT_NS;
   p.step_dev = (int*)(s + o_step);
   x->gen_dev = (int*)(s + o_gen);
@@ -516,7 +518,7 @@ static tinfer_status step_impl(tinfer_ctx* x, int token, const int* token_dev, i
     p.logits = logits; p.argmax = argmax;
     TRY_CUDA(launch_megakernel(p, x->smem_mega, st));
     x->p.dbg_skip_cta = -1;  // an injected fault applies to one step only
-    x->p.bar_base += (unsigned)(x->cfg.n_layers * PHASES_PER_LAYER) * (unsigned)x->p.grid;
+    x->p.epoch += (unsigned)(x->cfg.n_layers * PHASES_PER_LAYER + 2);  // fresh stamps for the next step
     return TINFER_OK;
   }
   if (!x->gexec || x->graph_logits != logits || x->graph_argmax != argmax)
@@ -546,8 +548,6 @@ tinfer_status tinfer_get_error(tinfer_ctx* x) {
   if (w || *reinterpret_cast<volatile int*>(x->err_host)) {
     uint8_t* s = (uint8_t*)x->scratch;
     TRY_CUDA(cudaMemset(s + x->err_off, 0, 4));
-    TRY_CUDA(cudaMemset(s + x->gbar_off, 0, 4));
-    x->p.bar_base = 0;
     TRY_CUDA(cudaMemset(s + x->tickets_off, 0, (size_t)(x->cfg.n_kv_heads + 1) * 4));
     TRY_CUDA(cudaDeviceSynchronize());
     *reinterpret_cast<volatile int*>(x->err_host) = 0;

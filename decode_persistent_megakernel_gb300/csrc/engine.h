@@ -74,16 +74,20 @@ struct __align__(16) StepParams {
   uint16_t* kcache;
   uint16_t* vcache;
   const float2* rope;      // [max_ctx][d/2] (cos, sin)
-  float* x;                // [H] residual stream
-  float* qkv;              // [qkv_rows]
-  float* attn;             // [nq * d]
-  float* act;              // [F]
+  // Activations handed from one phase to the next, as stamped words: the low 32 bits hold the fp32
+  // value, the high 32 bits the stamp of the phase that wrote it (epoch + phase index). A reader
+  // waits for the stamp it expects instead of for a grid barrier.
+  uint64_t* xa;            // [H] residual stream after the attention block of a layer
+  uint64_t* xb;            // [H] residual stream after the MLP block of a layer
+  uint64_t* qkv;           // [qkv_rows]
+  uint64_t* attn;          // [nq * d]
+  uint64_t* act;           // [F]
+  unsigned epoch;          // stamps of this launch: phase k writes epoch + k
+  int stamp_check;         // readers wait for the stamp (persistent kernel); 0: stream order suffices
   float* part_m;           // [nq][nch_cap]
   float* part_l;           // [nq][nch_cap]
   float* part_o;           // [nq][nch_cap][d]
   unsigned* tickets;       // [nkv + 1]: attention merge per KV head, then the argmax ticket
-  unsigned* gbar;          // [1]: grid barrier arrival counter (monotonic; wraps)
-  unsigned bar_base;       // counter value at the start of this launch
   float* best_val;         // [grid]
   int* best_idx;           // [grid]
   int* best_bad;           // [grid]
@@ -105,16 +109,16 @@ struct __align__(16) StepParams {
   int n_chunks_override;   // >0: fixed number of attention chunks (single-op test path)
   float* logits;           // [V] or null
   int* argmax;             // [1]
-  int dbg_skip_cta;        // fault injection: CTA that skips one grid-barrier arrival (-1 none)
-  int dbg_skip_barrier;
+  int dbg_skip_cta;        // fault injection: CTA that withholds its results of one GEMV phase (-1 none)
+  int dbg_skip_barrier;    // ... the phase index
   unsigned long long* trace;  // optional timeline [grid][phases][TRACE_FIELDS] of %globaltimer ns
 };
 
 // Timeline fields recorded per CTA and phase when StepParams::trace is set.
 enum TraceField : int {
-  TR_START = 0,      // consumers begin the phase (after the previous grid barrier)
+  TR_START = 0,      // consumers begin the phase
   TR_READY = 1,      // activations loaded (norm done): the stage loop starts
-  TR_END = 2,        // consumers done with the phase (before the grid barrier)
+  TR_END = 2,        // consumers done with the phase
   TR_PROD_BEGIN = 3, // producer starts issuing the phase's copies
   TR_PROD_END = 4,   // producer has issued the phase's last copy
   TR_ACT = 5,        // the phase's input activations are in registers (before the norm)

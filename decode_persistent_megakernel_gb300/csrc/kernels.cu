@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) op_gemv_kernel(const __grid_const
     pl.rs = rs;
     pl.src = ActSrc{};
     pl.src.xf = q.x; pl.src.gf = q.gain; pl.src.eps = q.eps; pl.src.n = q.cols;
-    pl.epi = Epi{q.epi, q.y, q.bias};
+    pl.epi = Epi{q.epi, q.y, q.bias, nullptr, 0u, 0};
     gemv_plan_finish(pp, pl, tid);
     Best best{-CUDART_INF_F, 0x7FFFFFFF, 0};
     gemv_consume_any(pp, pl, best, tid, nullptr);
@@ -85,7 +85,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) op_attention_kernel(const __grid_
       prod_drain(pp);
     }
   } else {
-    for (int u = blockIdx.x; u < units; u += gridDim.x) attn_unit(pp, A, sp, u / sp.nch, u % sp.nch, tid);
+    for (int u = blockIdx.x; u < units; u += gridDim.x)
+      if (!attn_unit(pp, A, sp, u / sp.nch, u % sp.nch, tid)) break;
     if (tid == 0) *reinterpret_cast<volatile int*>(&pp.ms->cons_done) = 1;
   }
   __syncthreads();

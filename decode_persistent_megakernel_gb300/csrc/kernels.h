@@ -57,6 +57,7 @@ cudaError_t set_smem_op_attention(size_t bytes);
 cudaError_t megakernel_occupancy(int* blocks_per_sm, size_t smem, int fmt, int nchl);
 cudaError_t phase_occupancy(int* blocks_per_sm, size_t smem, int fmt, int nchl);
 size_t smem_for(int stages, int slot, int xs_bytes);
+size_t static_smem_mega();  // static shared memory of the persistent kernel, with a margin
 
 cudaError_t launch_pack_rows(uint8_t* dst, int dst_rb, int dst_step, int dst_first, int rows,
                              const uint8_t* w, int w_bytes, const uint8_t* s, int s_bytes,

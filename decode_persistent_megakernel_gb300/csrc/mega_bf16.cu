@@ -6,4 +6,6 @@ namespace tinfer {
 
 TINFER_MEGA_INSTANCES(0, step_kernel_bf16)
 
+size_t static_smem_mega() { return sizeof(PhaseTable) + 256; }
+
 }  // namespace tinfer

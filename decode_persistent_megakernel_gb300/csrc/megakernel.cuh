@@ -45,10 +45,16 @@ __device__ __forceinline__ GemvDesc phase_gemv(const StepParams& p, int phase, i
   return g;
 }
 
-__device__ __forceinline__ AttnArgs step_attn_args(const StepParams& p, int layer, int pos) {
+// Attention of phase k (layer `layer`): q/k/v from the QKV phase k - 1, output for the O phase.
+__device__ __forceinline__ AttnArgs step_attn_args(const StepParams& p, int layer, int pos, int k) {
   const Dims& m = p.m;
   AttnArgs A;
-  A.qkv = p.qkv;
+  A.qkv = nullptr;
+  A.qkvw = p.qkv;
+  A.stamp_in = p.epoch + (unsigned)(k - 1);
+  A.check = p.stamp_check;
+  A.outw = p.attn;
+  A.stamp_out = p.epoch + (unsigned)k;
   const size_t lay = (size_t)layer * m.nkv * m.max_ctx * m.d;
   A.kc = p.kcache + lay;
   A.vc = p.vcache + lay;
@@ -58,7 +64,7 @@ __device__ __forceinline__ AttnArgs step_attn_args(const StepParams& p, int laye
   A.part_o = p.part_o;
   A.nch_cap = p.nch_cap;
   A.tickets = p.tickets;
-  A.out = p.attn;
+  A.out = nullptr;
   A.nq = m.nq; A.nkv = m.nkv; A.d = m.d; A.max_ctx = m.max_ctx; A.pos = pos;
   return A;
 }
@@ -66,7 +72,7 @@ __device__ __forceinline__ AttnArgs step_attn_args(const StepParams& p, int laye
 __device__ __forceinline__ void produce_phase(const StepParams& p, Pipe& pp, int phase, int layer, int pos,
                               uint64_t pol_w, uint64_t pol_kv, bool& dead) {
   if (phase == PH_ATTN) {
-    const AttnArgs A = step_attn_args(p, layer, pos);
+    const AttnArgs A = step_attn_args(p, layer, pos, 0);  // the producer uses the cache pointers only
     const AttnSplit sp = attn_split(pos, A.nkv, A.d, p.grid, p.slot_bytes, p.n_chunks_override);
     const int units = A.nkv * sp.nch;
     for (int u = blockIdx.x; u < units; u += p.grid)
@@ -228,140 +234,128 @@ __device__ __forceinline__ void produce_step(const StepParams& p, Pipe& pp, int 
 
 // Consumer side of one attention phase (every unit this CTA owns). Separate from the GEMV phase so
 // that each gets its own register allocation; the pipe state goes in and comes back by value.
-__device__ __forceinline__ Pipe consume_attn_phase(const StepParams& p, Pipe pp, int layer, int pos,
-                                                int tid, int k, unsigned long long* trace) {
+__device__ __forceinline__ bool consume_attn_phase(const StepParams& p, Pipe& pp, int layer, int pos,
+                                                   int tid, int k, unsigned long long* trace) {
   unsigned long long* tr_ready = trace_at(trace, p, k, TR_READY);
   if (tr_ready && tid == 0) *tr_ready = globaltimer();
-  const AttnArgs A = step_attn_args(p, layer, pos);
+  const AttnArgs A = step_attn_args(p, layer, pos, k);
   const AttnSplit sp = attn_split(pos, A.nkv, A.d, p.grid, p.slot_bytes, p.n_chunks_override);
   const int units = A.nkv * sp.nch;
   unsigned long long* tr = trace_at(trace, p, k, 0);  // the first unit of the CTA records sub-steps
   for (int u = blockIdx.x; u < units; u += p.grid) {
-    attn_unit(pp, A, sp, u / sp.nch, u % sp.nch, tid, tr);
+    if (!attn_unit(pp, A, sp, u / sp.nch, u % sp.nch, tid, tr)) return false;
     tr = nullptr;
   }
-  return pp;
+  return true;
+}
+
+// Per-launch shared-memory copy of what every GEMV phase's plan needs: the descriptor and this
+// CTA's row split of each of the five matrix kinds (the same for every layer) and the layer table.
+// Without it each phase start would recompute the split (integer divisions) and read the layer
+// table through the constant cache, whose misses cost about a microsecond per phase.
+struct PhaseTable {
+  GemvDesc desc[6];   // indexed by Phase (PH_ATTN unused); w = nullptr
+  RowSplit rs[6];
+  LayerDev layers[MAX_LAYERS];
+};
+__device__ __forceinline__ void fill_phase_table(const StepParams& p, PhaseTable& t, int tid) {
+  if (tid < 6 && tid != PH_ATTN) {
+    GemvDesc g = phase_gemv(p, tid, 0);
+    g.w = nullptr;
+    t.desc[tid] = g;
+    t.rs[tid] = row_split(g, blockIdx.x, p.grid, p.slot_bytes);
+  }
+  for (int l = tid; l < p.m.L; l += NCT) t.layers[l] = p.layers[l];
 }
 
 // The plan of a GEMV phase: QKV (RMSNorm prologue, bias), O (+ residual), gate/up (RMSNorm,
 // SwiGLU), down (+ residual) or the LM head (final RMSNorm, logits, argmax).
 __device__ __forceinline__ GemvPlan plan_gemv(const StepParams& p, Pipe& pp, int phase, int layer,
-                                              int token, int tid) {
+                                              int k, int token, int tid, const PhaseTable* tab) {
   const Dims& m = p.m;
   GemvPlan pl;
-  pl.g = phase_gemv(p, phase, layer);
-  pl.rs = row_split(pl.g, blockIdx.x, p.grid, p.slot_bytes);
-  const LayerDev& L = p.layers[layer];
+  const LayerDev& L = tab ? tab->layers[layer] : p.layers[layer];
+  if (tab) {
+    pl.g = tab->desc[phase];
+    pl.g.w = phase == PH_QKV ? L.qkv : phase == PH_O ? L.o : phase == PH_GU ? L.gu : phase == PH_DOWN
+             ? L.down : reinterpret_cast<const uint8_t*>(p.lm_head);
+    pl.rs = tab->rs[phase];
+  } else {
+    pl.g = phase_gemv(p, phase, layer);
+    pl.rs = row_split(pl.g, blockIdx.x, p.grid, p.slot_bytes);
+  }
   pl.src = ActSrc{};
   pl.src.eps = m.eps;
+  // phase k reads the stamped results of phase k - 1 and writes its own with stamp epoch + k
+  pl.src.stamp = p.epoch + (unsigned)(k - 1);
+  pl.src.check = p.stamp_check;
+  const unsigned own = p.epoch + (unsigned)k;
+  const uint16_t* erow = p.embed + (size_t)token * m.H;
   switch (phase) {
     case PH_QKV:
-      if (layer == 0) pl.src.xb = p.embed + (size_t)token * m.H; else pl.src.xf = p.x;
+      if (layer == 0) pl.src.xb = erow; else pl.src.xw = p.xb;
       pl.src.gf = L.g1; pl.src.n = m.H;
-      pl.epi = Epi{EK_STORE, p.qkv, L.bias};
+      pl.epi = Epi{EK_STORE, p.qkv, L.bias, nullptr, own, EF_OUT_STAMPED};
       break;
     case PH_O:
-      pl.src.xf = p.attn; pl.src.n = m.nq * m.d;
-      pl.epi = Epi{EK_RESIDUAL, p.x, nullptr};
+      pl.src.xw = p.attn; pl.src.n = m.nq * m.d;
+      if (layer == 0) pl.epi = Epi{EK_RESIDUAL, p.xa, nullptr, erow, own, EF_OUT_STAMPED | EF_RES_BF16};
+      else pl.epi = Epi{EK_RESIDUAL, p.xa, nullptr, p.xb, own, EF_OUT_STAMPED | EF_RES_STAMPED};
       break;
     case PH_GU:
-      pl.src.xf = p.x; pl.src.gf = L.g2; pl.src.n = m.H;
-      pl.epi = Epi{EK_SWIGLU, p.act, nullptr};
+      pl.src.xw = p.xa; pl.src.gf = L.g2; pl.src.n = m.H;
+      pl.epi = Epi{EK_SWIGLU, p.act, nullptr, nullptr, own, EF_OUT_STAMPED};
       break;
     case PH_DOWN:
-      pl.src.xf = p.act; pl.src.n = m.F;
-      pl.epi = Epi{EK_RESIDUAL, p.x, nullptr};
+      pl.src.xw = p.act; pl.src.n = m.F;
+      pl.epi = Epi{EK_RESIDUAL, p.xb, nullptr, p.xa, own, EF_OUT_STAMPED | EF_RES_STAMPED};
       break;
     default:
-      pl.src.xf = p.x; pl.src.gb = p.final_norm; pl.src.n = m.H;
-      pl.epi = Epi{EK_ARGMAX, p.logits, nullptr};
+      pl.src.xw = p.xb; pl.src.gb = p.final_norm; pl.src.n = m.H;
+      pl.epi = Epi{EK_ARGMAX, p.logits, nullptr, nullptr, own, 0};
       break;
   }
+  if (p.dbg_skip_cta == (int)blockIdx.x && p.dbg_skip_barrier == k) pl.epi.flags |= EF_WITHHOLD;
   gemv_plan_finish(pp, pl, tid);
   return pl;
 }
 
-// Consumer side of one GEMV phase from its plan.
+// Consumer side of one GEMV phase from its plan; false when its input never showed up.
 template <int FMT, int NCHL>
-__device__ __forceinline__ void run_gemv_phase(const StepParams& p, Pipe& pp, const GemvPlan& pl,
-                                               int phase, int layer, int token, int tid, int k,
-                                               unsigned long long* trace) {
+__device__ __forceinline__ bool run_gemv_phase(const StepParams& p, Pipe& pp, const GemvPlan& pl,
+                                               int phase, int tid, int k, unsigned long long* trace) {
   const Dims& m = p.m;
   unsigned long long* tr_ready = trace_at(trace, p, k, TR_READY);
   Best best{-CUDART_INF_F, 0x7FFFFFFF, 0};
   // int4 models stream their linears as int4 and the LM head as bf16; bf16 models need one format
-  if (FMT == 1 && pl.g.fmt == 1) gemv_rows<1, 2>(pp, pl, best, tid, tr_ready);
-  else gemv_rows<0, NCHL>(pp, pl, best, tid, tr_ready);
-  if (phase == PH_QKV && layer == 0 && blockIdx.x == 0)
-    for (int i = tid; i < m.H; i += NCT) p.x[i] = bf16_to_f(p.embed[(size_t)token * m.H + i]);
+  const bool ok = (FMT == 1 && pl.g.fmt == 1) ? gemv_rows<1, 2>(pp, pl, best, tid, tr_ready)
+                                              : gemv_rows<0, NCHL>(pp, pl, best, tid, tr_ready);
+  if (!ok) return false;
   if (phase == PH_LM) {
     const Best cb = best_block_reduce(best, pp.ms, tid);
     argmax_publish(cb, p.best_val, p.best_idx, p.best_bad, p.tickets + m.nkv, p.grid, blockIdx.x,
                    p.argmax, p.err, p.err_host, pp.ms, tid);
   }
+  return true;
 }
 
-// Phase k: its plan (GEMV phases) and its run. The persistent kernel calls plan_phase for phase
-// k + 1 before the grid barrier that ends phase k.
+// Phase k: its plan (GEMV phases) and its run.
 __device__ __forceinline__ GemvPlan plan_phase(const StepParams& p, Pipe& pp, int k, int token,
-                                               int tid) {
+                                               int tid, const PhaseTable* tab = nullptr) {
   int phase, layer;
   phase_of(k, p.m.L, phase, layer);
   if (phase == PH_ATTN) return GemvPlan{};
-  return plan_gemv(p, pp, phase, layer, token, tid);
+  return plan_gemv(p, pp, phase, layer, k, token, tid, tab);
 }
 
 template <int FMT, int NCHL>
-__device__ __forceinline__ void run_phase(const StepParams& p, Pipe& pp, const GemvPlan& pl, int k,
+__device__ __forceinline__ bool run_phase(const StepParams& p, Pipe& pp, const GemvPlan& pl, int k,
                                           int token, int pos, int tid, unsigned long long* trace) {
+  (void)token;
   int phase, layer;
   phase_of(k, p.m.L, phase, layer);
-  if (phase == PH_ATTN) pp = consume_attn_phase(p, pp, layer, pos, tid, k, trace);
-  else run_gemv_phase<FMT, NCHL>(p, pp, pl, phase, layer, token, tid, k, trace);
-}
-
-// Barrier over the CTAs of the cooperative launch, run by the consumer warps: one monotonic
-// arrival counter (it never resets; barrier k of a launch waits for bar_base + (k+1) * grid).
-// It is split in two so that work which needs no other CTA's results (the next phase's plan) runs
-// between the arrival and the wait. grid_arrive: after all consumer threads are done, thread 0
-// arrives with a release reduction that publishes the CTA's writes. It returns, in thread 0, 0 when
-// it arrived, 1 when the step must stop, 2 when fault injection skipped the arrival.
-__device__ __forceinline__ int grid_arrive(const StepParams& p, Misc* ms, int tid, int index) {
-  named_sync(BAR_CONS, NCT);
-  int state = 0;
-  if (tid == 0) {
-    if (*reinterpret_cast<volatile int*>(&ms->abort)) state = 1;
-    else if (p.dbg_skip_cta == (int)blockIdx.x && p.dbg_skip_barrier == index) state = 2;
-    else red_add_release(p.gbar, 1u);
-  }
-  return state;
-}
-
-// grid_wait: thread 0 polls with acquire loads until the counter reaches the barrier's target,
-// under a time limit; the poll also ends when another CTA has raised an error. Returns false, the
-// same in every consumer thread, when the step must stop.
-__device__ __forceinline__ bool grid_wait(const StepParams& p, Misc* ms, int tid, int index, int state) {
-  if (tid == 0) {
-    int stop = state == 1;
-    if (state == 0) {
-      const unsigned target = p.bar_base + (unsigned)(index + 1) * (unsigned)p.grid;
-      const uint64_t t0 = globaltimer();
-      unsigned spins = 0;
-      while ((int)(ld_acquire(p.gbar) - target) < 0) {
-        if ((++spins & 63u) == 0) {
-          if (ld_volatile_int(p.err) != 0) { stop = 1; break; }
-          if ((long long)(globaltimer() - t0) > p.timeout_ns) {
-            raise_error(p.err, p.err_host, EW_TIMEOUT);
-            stop = 1;
-            break;
-          }
-        }
-      }
-    }
-    ms->exit_now = stop;
-  }
-  named_sync(BAR_CONS, NCT);
-  return !*reinterpret_cast<volatile int*>(&ms->exit_now);
+  if (phase == PH_ATTN) return consume_attn_phase(p, pp, layer, pos, tid, k, trace);
+  return run_gemv_phase<FMT, NCHL>(p, pp, pl, phase, tid, k, trace);
 }
 
 // Start-of-step decision, identical in every CTA: skip when an earlier step left an error, or when
@@ -388,6 +382,7 @@ __global__ void __launch_bounds__(NTHREADS_MEGA, 1) decode_megakernel(const __gr
   unsigned long long* const trace = TRACE ? p.trace : nullptr;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ int s_tok[2];
+  __shared__ PhaseTable s_tab;
   Pipe pp;
   pipe_init(pp, smem, p.ring_stages, p.slot_bytes, p.timeout_ns, p.err, p.err_host);
   pp.inflight = p.inflight;
@@ -402,16 +397,16 @@ __global__ void __launch_bounds__(NTHREADS_MEGA, 1) decode_megakernel(const __gr
     if (tid == NCT) produce_step(p, pp, pos, trace);
   } else {
     reg_alloc<REG_CONSUMER>();
-    GemvPlan plan = plan_phase(p, pp, 0, token, tid);
+    // no grid barrier: each phase waits, inside its input fetch, for the stamps of the results it
+    // reads, so a CTA starts a phase as soon as its own inputs are complete
+    fill_phase_table(p, s_tab, tid);
+    named_sync(BAR_CONS, NCT);
     for (int k = 0; k < nph; ++k) {
       if (unsigned long long* t = trace_at(trace, p, k, TR_START)) if (tid == 0) *t = globaltimer();
-      run_phase<FMT, NCHL>(p, pp, plan, k, token, pos, tid, trace);
+      const GemvPlan plan = plan_phase(p, pp, k, token, tid, &s_tab);
+      const bool ok = run_phase<FMT, NCHL>(p, pp, plan, k, token, pos, tid, trace);
       if (unsigned long long* t = trace_at(trace, p, k, TR_END)) if (tid == 0) *t = globaltimer();
-      if (k + 1 < nph) {
-        const int st = grid_arrive(p, pp.ms, tid, k);
-        plan = plan_phase(p, pp, k + 1, token, tid);  // overlaps the barrier wait
-        if (!grid_wait(p, pp.ms, tid, k, st)) break;
-      }
+      if (!ok) break;
     }
     if (tid == 0) *reinterpret_cast<volatile int*>(&pp.ms->cons_done) = 1;
   }
@@ -446,7 +441,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) decode_phase_kernel(const __grid_
     if (!*reinterpret_cast<volatile int*>(&pp.ms->exit_now)) {
       const int token = p.step_dev[0], pos = p.step_dev[1];
       const GemvPlan plan = plan_phase(p, pp, k, token, tid);  // after the wait: reads x of the previous kernel
-      run_phase<FMT, NCHL>(p, pp, plan, k, token, pos, tid, p.trace);
+      (void)run_phase<FMT, NCHL>(p, pp, plan, k, token, pos, tid, p.trace);
     }
     named_sync(BAR_CONS, NCT);
     if (tid == 0) *reinterpret_cast<volatile int*>(&pp.ms->cons_done) = 1;

@@ -213,6 +213,44 @@ __device__ __forceinline__ uint16_t f_to_bf16_bits(float v) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
+// ---- stamped words: fp32 value in the low half, the writing phase's stamp in the high half -------
+__device__ __forceinline__ uint64_t stamp_word(float v, unsigned stamp) {
+  return ((uint64_t)stamp << 32) | (uint64_t)__float_as_uint(v);
+}
+__device__ __forceinline__ float word_value(uint64_t w) { return __uint_as_float((uint32_t)w); }
+__device__ __forceinline__ unsigned word_stamp(uint64_t w) { return (unsigned)(w >> 32); }
+
+// Bounded polling of stamped words another CTA writes: again() is called after each stale read; it
+// returns false once the time limit has passed (raising the time-out error) or another CTA has
+// raised an error, and then sets the CTA's abort flag.
+struct Poll {
+  uint64_t t0 = 0;
+  unsigned n = 0;
+  __device__ __forceinline__ bool again(const Pipe& pp) {
+    if (n++ == 0) t0 = globaltimer();
+    if ((n & 15u) == 0) {
+      volatile int* ab = &pp.ms->abort;
+      if (*ab || ld_volatile_int(pp.err) != 0) { *ab = 1; return false; }
+      if ((long long)(globaltimer() - t0) > pp.timeout) {
+        raise_error(pp.err, pp.err_host, EW_TIMEOUT);
+        *ab = 1;
+        return false;
+      }
+    }
+    return true;
+  }
+};
+
+// The value of a stamped word once it carries `stamp` (with check; else as read).
+__device__ __forceinline__ float await_word(const uint64_t* p, unsigned stamp, bool check, const Pipe& pp) {
+  uint64_t w = __ldcg(reinterpret_cast<const unsigned long long*>(p));
+  if (check) {
+    Poll pl;
+    while (word_stamp(w) != stamp && pl.again(pp)) w = __ldcg(reinterpret_cast<const unsigned long long*>(p));
+  }
+  return word_value(w);
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
@@ -304,8 +342,11 @@ __device__ __forceinline__ float dot32_int4(const uint4 w, const float* a) {
 
 // Where the activation vector of a GEMV comes from.
 struct ActSrc {
-  const float* xf;     // fp32 source (read through L2: other CTAs wrote it in this launch)
-  const uint16_t* xb;  // or bf16 source (the embedding row)
+  const float* xf;     // fp32 source (single-operation path), or
+  const uint64_t* xw;  // stamped words another phase wrote (read through L2), or
+  const uint16_t* xb;  // bf16 source (the embedding row)
+  unsigned stamp;      // stamp the words must carry (xw)
+  int check;           // wait for the stamp (xw)
   const float* gf;     // fp32 RMSNorm gain, or
   const uint16_t* gb;  // bf16 RMSNorm gain, or neither (no norm)
   float eps;
@@ -334,9 +375,26 @@ __device__ __forceinline__ RowSplit row_split(const GemvDesc& g, int cta, int gr
 enum EpiKind : int { EK_STORE = 0, EK_RESIDUAL = 1, EK_SWIGLU = 2, EK_ARGMAX = 3 };
 struct Epi {
   int kind;
-  float* y;
+  void* out;              // output: plain floats (single operations, logits) or stamped words
   const float* bias;
+  const void* res;        // EK_RESIDUAL input: null (out itself), stamped words or bf16 (flags)
+  unsigned stamp;         // stamp of stamped output words
+  int flags;              // EF_* below
 };
+enum : int { EF_OUT_STAMPED = 1, EF_RES_STAMPED = 2, EF_RES_BF16 = 4, EF_WITHHOLD = 8 };
+
+// Residual input of row r (EK_RESIDUAL): the rows are this thread's own, written by it in an
+// earlier phase (or constant), so no stamp needs checking.
+__device__ __forceinline__ float residual_at(const Epi& e, int r) {
+  if (e.flags & EF_RES_STAMPED) return word_value(static_cast<const uint64_t*>(e.res)[r]);
+  if (e.flags & EF_RES_BF16) return bf16_to_f(static_cast<const uint16_t*>(e.res)[r]);
+  return __ldcg(static_cast<const float*>(e.out) + r);
+}
+__device__ __forceinline__ void epi_write(const Epi& e, int r, float v) {
+  if (e.flags & EF_WITHHOLD) return;
+  if (e.flags & EF_OUT_STAMPED) static_cast<uint64_t*>(e.out)[r] = stamp_word(v, e.stamp);
+  else static_cast<float*>(e.out)[r] = v;
+}
 
 struct Best {
   float v;
@@ -365,7 +423,8 @@ __device__ __forceinline__ float4 gain_block(const ActSrc& src, int j) {
 // the CTA's own bulk weight copies. With an RMSNorm gain the stored values are x * g (the first
 // GAIN_PRE gain blocks of the thread come from `gpre`, loaded before the barrier) and the sum of
 // squares of x is reduced on the way; the return value is 1 / rms(x) (1 without a norm), the same in
-// every consumer thread. Returns after the named barrier that publishes the copy.
+// every consumer thread. Returns after the named barrier that publishes the copy; the CTA's abort
+// flag is then set (the same in every thread) if a stamped source never showed up.
 __device__ __forceinline__ float fetch_vector(Pipe& pp, const ActSrc& src, const float4* gpre, int tid) {
   const bool norm = src.gf || src.gb;
   const int nb = src.n / 4;
@@ -373,7 +432,38 @@ __device__ __forceinline__ float fetch_vector(Pipe& pp, const ActSrc& src, const
   float ss = 0.f;
   for (int j0 = tid, turn = 0; j0 < nb; j0 += FETCH_IF * NCT, ++turn) {
     float4 x[FETCH_IF];
-    if (src.xf) {
+    if (src.xw) {
+      // two 16-byte loads per block of 4 stamped words; stale blocks are read again until their
+      // writers' stamps show (bounded)
+      const ulonglong2* xw = reinterpret_cast<const ulonglong2*>(src.xw);
+      ulonglong2 w0[FETCH_IF], w1[FETCH_IF];
+#pragma unroll
+      for (int u = 0; u < FETCH_IF; ++u) {
+        const int j = j0 + u * NCT;
+        if (j < nb) {
+          w0[u] = __ldcg(xw + 2 * j);
+          w1[u] = __ldcg(xw + 2 * j + 1);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < FETCH_IF; ++u) {
+        const int j = j0 + u * NCT;
+        if (j < nb) {
+          if (src.check) {
+            const unsigned sv = src.stamp;
+            Poll pl;
+            while ((word_stamp(w0[u].x) != sv || word_stamp(w0[u].y) != sv || word_stamp(w1[u].x) != sv ||
+                    word_stamp(w1[u].y) != sv) && pl.again(pp)) {
+              w0[u] = __ldcg(xw + 2 * j);
+              w1[u] = __ldcg(xw + 2 * j + 1);
+            }
+          }
+          x[u] = make_float4(word_value(w0[u].x), word_value(w0[u].y), word_value(w1[u].x), word_value(w1[u].y));
+        } else {
+          x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+    } else if (src.xf) {
       const float4* xf = reinterpret_cast<const float4*>(src.xf);
 #pragma unroll
       for (int u = 0; u < FETCH_IF; ++u) {
@@ -467,35 +557,18 @@ struct GemvPlan {
   RowSplit rs;
   ActSrc src;
   Epi epi;
-  float pre;     // epilogue operand of row rs.r0 + tid (residual x or bias), fetched early
-  float4 gpre[GAIN_PRE];  // RMSNorm gain blocks tid + u * NCT this thread multiplies in
 };
 
 // Completes a plan whose g, rs, src and epi are set: loads the early epilogue operand (the residual
 // rows are this CTA's own from its previous write, or the constant bias) and the thread's RMSNorm
 // gain blocks (constants: their first touch may miss to HBM, which the barrier wait then hides).
 __device__ __forceinline__ void gemv_plan_finish(Pipe& pp, GemvPlan& pl, int tid) {
-  const SegInfo si = seg_info(pl.g.fmt, pl.g.cols);
-  const int nrows = pl.rs.r1 - pl.rs.r0;
-  const bool direct = pl.epi.kind == EK_ARGMAX && si.nseg == 1;
-  pl.pre = 0.f;
-  if (!direct && tid < nrows && pl.epi.kind != EK_ARGMAX) {
-    if (pl.epi.kind == EK_RESIDUAL) pl.pre = __ldcg(pl.epi.y + pl.rs.r0 + tid);
-    else if (pl.epi.kind == EK_STORE && pl.epi.bias) pl.pre = __ldg(pl.epi.bias + pl.rs.r0 + tid);
-  }
   (void)pp;
-  if (pl.src.gf || pl.src.gb) {
-    const int nb = pl.src.n / 4;
-#pragma unroll
-    for (int u = 0; u < GAIN_PRE; ++u) {
-      const int j = tid + u * NCT;
-      pl.gpre[u] = j < nb ? gain_block(pl.src, j) : make_float4(1.f, 1.f, 1.f, 1.f);
-    }
-  }
+  (void)tid;
 }
 
 template <int FMT, int NCHL>
-__device__ void gemv_rows(Pipe& pp, const GemvPlan& pl, Best& best, int tid,
+__device__ __forceinline__ bool gemv_rows(Pipe& pp, const GemvPlan& pl, Best& best, int tid,
                           unsigned long long* tr_ready) {
   constexpr int E = FMT == 0 ? 8 : 32;
   const GemvDesc& g = pl.g;
@@ -510,14 +583,20 @@ __device__ void gemv_rows(Pipe& pp, const GemvPlan& pl, Best& best, int tid,
   const int nrows = rs.r1 - rs.r0;
   const bool direct = epi.kind == EK_ARGMAX && si.nseg == 1;  // the warp holds whole rows
   const bool norm = src.gf || src.gb;
-  const float pre = pl.pre;
+  // epilogue operand of row rs.r0 + tid, loaded now so that its latency hides under the fetch
+  float pre = 0.f;
+  if (!direct && tid < nrows && epi.kind != EK_ARGMAX) {
+    if (epi.kind == EK_RESIDUAL) pre = residual_at(epi, rs.r0 + tid);
+    else if (epi.kind == EK_STORE && epi.bias) pre = __ldg(epi.bias + rs.r0 + tid);
+  }
 
   // the input vector (x * g for RMSNorm phases) into shared memory, then this warp's segment into
   // registers, scaled by 1 / rms(x); chunks past the segment read the segment's last chunk slot and
   // are zeroed, so that the row loop needs no per-lane branches
   if (tr_ready && tid == 0) tr_ready[TR_ENTRY - TR_READY] = globaltimer();
-  const float inv = fetch_vector(pp, src, pl.gpre, tid);
+  const float inv = fetch_vector(pp, src, nullptr, tid);
   if (tr_ready && tid == 0) tr_ready[TR_FETCHED - TR_READY] = globaltimer();
+  if (*reinterpret_cast<volatile int*>(&pp.ms->abort)) return false;  // uniform after the fetch
   (void)norm;
   float a[NCHL][E];
   float S[NCHL];
@@ -581,7 +660,7 @@ __device__ void gemv_rows(Pipe& pp, const GemvPlan& pl, Best& best, int tid,
       const int rl = (n / m) * rs.nr + grp + (n % m) * WG;
       if (direct) {
         const int r = rs.r0 + rl;
-        if (epi.y) epi.y[r] = v;
+        if (epi.out) static_cast<float*>(epi.out)[r] = v;
         best_update(best, v, r);
       } else {
         ms->rowv[rl * si.nseg + seg] = v;
@@ -623,14 +702,14 @@ __device__ void gemv_rows(Pipe& pp, const GemvPlan& pl, Best& best, int tid,
     cons_release(pp, lane);
   }
   if (filled) flush();
-  if (direct) return;
+  if (direct) return true;
   named_sync(BAR_CONS, NCT);
   if (epi.kind == EK_SWIGLU) {
     for (int p = tid; p < nrows / 2; p += NCT) {
       float gt = 0.f, up = 0.f;
       for (int s2 = 0; s2 < si.nseg; ++s2) gt += ms->rowv[(2 * p) * si.nseg + s2];
       for (int s2 = 0; s2 < si.nseg; ++s2) up += ms->rowv[(2 * p + 1) * si.nseg + s2];
-      epi.y[rs.r0 / 2 + p] = gt / (1.f + expf(-gt)) * up;
+      epi_write(epi, rs.r0 / 2 + p, gt / (1.f + expf(-gt)) * up);
     }
   } else {
     for (int t = tid; t < nrows; t += NCT) {
@@ -638,29 +717,27 @@ __device__ void gemv_rows(Pipe& pp, const GemvPlan& pl, Best& best, int tid,
       for (int s2 = 0; s2 < si.nseg; ++s2) v += ms->rowv[t * si.nseg + s2];
       const int r = rs.r0 + t;
       if (epi.kind == EK_ARGMAX) {
-        if (epi.y) epi.y[r] = v;
+        if (epi.out) static_cast<float*>(epi.out)[r] = v;
         best_update(best, v, r);
         continue;
       }
       float base = pre;
-      if (t >= NCT) base = epi.kind == EK_RESIDUAL ? __ldcg(epi.y + r) : (epi.bias ? epi.bias[r] : 0.f);
-      epi.y[r] = (epi.kind == EK_RESIDUAL || epi.bias) ? base + v : v;
+      if (t >= NCT) base = epi.kind == EK_RESIDUAL ? residual_at(epi, r) : (epi.bias ? epi.bias[r] : 0.f);
+      epi_write(epi, r, (epi.kind == EK_RESIDUAL || epi.bias) ? base + v : v);
     }
   }
+  return true;
 }
 
 // Dispatch to the instance of the weight format and chunk count per lane (rounded up to even).
-__device__ __forceinline__ void gemv_consume_any(Pipe& pp, const GemvPlan& pl, Best& best, int tid,
+__device__ __forceinline__ bool gemv_consume_any(Pipe& pp, const GemvPlan& pl, Best& best, int tid,
                                                  unsigned long long* tr_ready) {
-  if (pl.g.fmt == 1) {
-    gemv_rows<1, 2>(pp, pl, best, tid, tr_ready);
-    return;
-  }
+  if (pl.g.fmt == 1) return gemv_rows<1, 2>(pp, pl, best, tid, tr_ready);
   const int nchl = (seg_info(0, pl.g.cols).chs + 31) / 32;
-  if (nchl > 6) gemv_rows<0, 8>(pp, pl, best, tid, tr_ready);
-  else if (nchl > 4) gemv_rows<0, 6>(pp, pl, best, tid, tr_ready);
-  else if (nchl > 2) gemv_rows<0, 4>(pp, pl, best, tid, tr_ready);
-  else gemv_rows<0, 2>(pp, pl, best, tid, tr_ready);
+  if (nchl > 6) return gemv_rows<0, 8>(pp, pl, best, tid, tr_ready);
+  if (nchl > 4) return gemv_rows<0, 6>(pp, pl, best, tid, tr_ready);
+  if (nchl > 2) return gemv_rows<0, 4>(pp, pl, best, tid, tr_ready);
+  return gemv_rows<0, 2>(pp, pl, best, tid, tr_ready);
 }
 
 __device__ __forceinline__ void produce_rows(Pipe& pp, const GemvDesc& g, const RowSplit& rs,
@@ -765,7 +842,12 @@ __device__ __forceinline__ AttnSplit attn_split(int pos, int nkv, int d, int gri
 }
 
 struct AttnArgs {
-  const float* qkv;        // [q | k | v] raw projections
+  const float* qkv;        // [q | k | v] raw projections (single operation), or
+  const uint64_t* qkvw = nullptr;  // the same as stamped words (the step): wait for stamp_in
+  unsigned stamp_in = 0;
+  int check = 0;
+  uint64_t* outw = nullptr;        // stamped output (the step), written with stamp_out
+  unsigned stamp_out = 0;
   uint16_t* kc;            // this layer's K cache [nkv][max_ctx][d]
   uint16_t* vc;
   const float2* rope;      // [max_ctx][d/2]
@@ -848,7 +930,9 @@ static __device__ void attn_merge(const AttnArgs& A, Misc* ms, int tid, int j, i
 #pragma unroll
       for (int u = 0; u < MB; ++u) acc = c + u < nch ? fmaf(wg[c + u], ob[u], acc) : acc;
     }
-    A.out[(size_t)(j * G + g) * d + i] = acc * ms->hl[g];
+    const size_t oi = (size_t)(j * G + g) * d + i;
+    if (A.outw) A.outw[oi] = stamp_word(acc * ms->hl[g], A.stamp_out);
+    else A.out[oi] = acc * ms->hl[g];
   }
 }
 
@@ -968,7 +1052,7 @@ __device__ __forceinline__ void attn_scores_threads(uint32_t kst, const float* q
 // tr: optional timeline row of the phase (fields TR_READY, TR_ACT, TR_ENTRY, TR_AUX0, TR_FETCHED,
 // TR_AUX1 receive the keys' arrival, the ends of the query set-up and the scores, the values'
 // arrival, the end of the partials and the merge start).
-static __device__ void attn_unit(Pipe& pp, const AttnArgs& A, const AttnSplit& sp, int j, int c, int tid,
+static __device__ bool attn_unit(Pipe& pp, const AttnArgs& A, const AttnSplit& sp, int j, int c, int tid,
                                  unsigned long long* tr = nullptr) {
   Misc* ms = pp.ms;
   const int lane = tid & 31, warp = tid >> 5;
@@ -981,25 +1065,62 @@ static __device__ void attn_unit(Pipe& pp, const AttnArgs& A, const AttnSplit& s
   const int T = max(0, t1 - t0);             // positions of the chunk: nk, plus pos itself
   const float scale = 1.f / sqrtf((float)d);
   const float2* rt = A.rope + (size_t)pos * half;
-  const float* q = A.qkv + (size_t)j * G * d;
-  const float* kr = A.qkv + (size_t)A.nq * d + (size_t)j * d;
-  const float* vr = kr + (size_t)A.nkv * d;
+  const size_t qo = (size_t)j * G * d;                      // q of the group's heads
+  const size_t ko = (size_t)A.nq * d + (size_t)j * d;       // k of KV head j
+  const size_t vo = ko + (size_t)A.nkv * d;                 // v of KV head j
+  // inputs: every load is issued first (stamped words, or plain floats as their bits), then each is
+  // settled -- for stamped words by waiting for the stamp of the QKV phase
+  auto raw = [&](size_t i) -> uint64_t {
+    return A.qkvw ? (uint64_t)__ldcg(reinterpret_cast<const unsigned long long*>(A.qkvw + i))
+                  : (uint64_t)__float_as_uint(__ldcg(A.qkv + i));
+  };
+  auto settle = [&](uint64_t w, size_t i) -> float {
+    if (A.qkvw && A.check) {
+      Poll pl;
+      while (word_stamp(w) != A.stamp_in && pl.again(pp))
+        w = __ldcg(reinterpret_cast<const unsigned long long*>(A.qkvw + i));
+    }
+    return word_value(w);
+  };
   float* qs = sptr_w<float>(smem_addr(ms->qs));
   float* sc = sptr_w<float>(smem_addr(ms->sc));
   float* kn = sptr_w<float>(smem_addr(ms->kn));
   float* vn = sptr_w<float>(smem_addr(ms->vn));
 
-  for (int idx = tid; idx < G * half; idx += NCT) {
-    const int g = idx / half, i = idx - g * half;
-    const float x0 = __ldcg(q + g * d + i), x1 = __ldcg(q + g * d + i + half);
-    const float2 cs = rt[i];
-    qs[g * d + i] = (x0 * cs.x - x1 * cs.y) * scale;
-    qs[g * d + i + half] = (x1 * cs.x + x0 * cs.y) * scale;
+  constexpr int QR = (G_MAX * D_MAX / 2 + NCT - 1) / NCT;  // query pairs per thread, at most
+  uint64_t wq[QR][2];
+  size_t iq[QR][2];
+#pragma unroll
+  for (int r = 0; r < QR; ++r) {
+    const int idx = tid + r * NCT;
+    if (idx < G * half) {
+      const int g = idx / half, i = idx - g * half;
+      iq[r][0] = qo + g * d + i;
+      iq[r][1] = qo + g * d + i + half;
+      wq[r][0] = raw(iq[r][0]);
+      wq[r][1] = raw(iq[r][1]);
+    }
+  }
+  const bool hk = has_pos && tid < half, hv = has_pos && tid < d;
+  uint64_t wk0 = 0, wk1 = 0, wv = 0;
+  if (hk) { wk0 = raw(ko + tid); wk1 = raw(ko + tid + half); }
+  if (hv) wv = raw(vo + tid);
+#pragma unroll
+  for (int r = 0; r < QR; ++r) {
+    const int idx = tid + r * NCT;
+    if (idx < G * half) {
+      const int g = idx / half, i = idx - g * half;
+      const float x0 = settle(wq[r][0], iq[r][0]), x1 = settle(wq[r][1], iq[r][1]);
+      const float2 cs = rt[i];
+      qs[g * d + i] = (x0 * cs.x - x1 * cs.y) * scale;
+      qs[g * d + i + half] = (x1 * cs.x + x0 * cs.y) * scale;
+    }
   }
   if (has_pos) {
     const size_t slot = ((size_t)j * A.max_ctx + pos) * d;
-    for (int i = tid; i < half; i += NCT) {
-      const float x0 = __ldcg(kr + i), x1 = __ldcg(kr + i + half);
+    if (hk) {
+      const int i = tid;
+      const float x0 = settle(wk0, ko + i), x1 = settle(wk1, ko + i + half);
       const float2 cs = rt[i];
       const uint16_t b0 = f_to_bf16_bits(x0 * cs.x - x1 * cs.y);
       const uint16_t b1 = f_to_bf16_bits(x1 * cs.x + x0 * cs.y);
@@ -1008,14 +1129,15 @@ static __device__ void attn_unit(Pipe& pp, const AttnArgs& A, const AttnSplit& s
       kn[i] = bf16_to_f(b0);
       kn[i + half] = bf16_to_f(b1);
     }
-    for (int i = tid; i < d; i += NCT) {
-      const uint16_t b = f_to_bf16_bits(__ldcg(vr + i));
-      A.vc[slot + i] = b;
-      vn[i] = bf16_to_f(b);
+    if (hv) {
+      const uint16_t b = f_to_bf16_bits(settle(wv, vo + tid));
+      A.vc[slot + tid] = b;
+      vn[tid] = bf16_to_f(b);
     }
   }
   named_sync(BAR_CONS, NCT);
   if (tr && tid == 0) tr[TR_ACT] = globaltimer();
+  if (*reinterpret_cast<volatile int*>(&ms->abort)) return false;  // inputs never showed up
 
   // ---- scores
   const uint32_t kst = cons_acquire(pp);
@@ -1097,6 +1219,7 @@ static __device__ void attn_unit(Pipe& pp, const AttnArgs& A, const AttnSplit& s
     if (tid == 0) atomicExch(A.tickets + j, 0u);
   }
   named_sync(BAR_CONS, NCT);
+  return true;
 }
 
 }  // namespace tinfer

@@ -156,9 +156,10 @@ long long tinfer_query(const tinfer_ctx* ctx, int what);
 tinfer_status tinfer_set_trace(tinfer_ctx* ctx, void* trace_dev);
 
 /* Test hooks: timeout of every device-side wait in nanoseconds (default 200 ms), and a fault
- * injected on the host side of the contract: CTA `cta` skips its arrival at grid barrier number
- * `barrier` of the next persistent step, so that the other CTAs' waits run out and the step
- * reports TINFER_ERR_TIMEOUT (cta = -1 disables). */
+ * injected on the host side of the contract: in the next persistent step, CTA `cta` withholds its
+ * results of GEMV phase number `barrier` (k = 5*layer + {0 QKV, 2 O, 3 gate/up, 4 down}; the LM head
+ * 5*n_layers), so that the CTAs waiting for them run out of time and the step reports
+ * TINFER_ERR_TIMEOUT (cta = -1 disables; a CTA without rows in that phase withholds nothing). */
 tinfer_status tinfer_set_timeout_ns(tinfer_ctx* ctx, long long ns);
 tinfer_status tinfer_debug_skip_barrier(tinfer_ctx* ctx, int cta, int barrier);
 

@@ -168,8 +168,9 @@ def test_nonfinite_logit_sets_error_word_then_recovers(mode):
 
 
 def test_barrier_timeout_is_reported_and_the_context_recovers():
-    # a fault made on the host side of the contract: one CTA skips one grid-barrier arrival, the
-    # other CTAs' bounded waits run out, the step ends with TINFER_ERR_TIMEOUT and the GPU stays usable
+    # a fault made on the host side of the contract: one CTA withholds its results of one phase, the
+    # bounded waits of the CTAs that need them run out, the step ends with TINFER_ERR_TIMEOUT and the
+    # GPU stays usable
     c = synth.config("tiny", max_ctx=8)
     w = synth.make_model(c)
     eng = T.Engine(c, w)
