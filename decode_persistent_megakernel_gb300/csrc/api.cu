@@ -370,6 +370,8 @@ tinfer_status tinfer_create(const tinfer_config* c, const tinfer_weights* w, voi
   const size_t o_attn = take((size_t)nq * d * 8), o_act = take((size_t)F * 8);
   const size_t o_pm = take((size_t)nq * nch_cap * 4), o_pl = take((size_t)nq * nch_cap * 4);
   const size_t o_po = take((size_t)nq * nch_cap * d * 4);
+  const size_t o_pmw = take((size_t)nq * nch_cap * 8), o_plw = take((size_t)nq * nch_cap * 8);
+  const size_t o_pow = take((size_t)nq * nch_cap * d * 8);
   const size_t o_tk = take((size_t)(nkv + 1) * 4);
   const size_t o_bv = take((size_t)grid * 4), o_bi = take((size_t)grid * 4), o_bb = take((size_t)grid * 4);
   const size_t o_err = take(4), o_step = take(2 * 4), o_gen = take(2 * 4), o_am = take(4);
@@ -423,6 +425,7 @@ tinfer_status tinfer_create(const tinfer_config* c, const tinfer_weights* w, voi
   p.epoch = 1;  // the buffers start zeroed: stamp 0 is never expected
   p.stamp_check = c->exec_mode == TINFER_MEGAKERNEL;
   p.part_m = (float*)(s + o_pm); p.part_l = (float*)(s + o_pl); p.part_o = (float*)(s + o_po);
+  p.part_mw = (uint64_t*)(s + o_pmw); p.part_lw = (uint64_t*)(s + o_plw); p.part_ow = (uint64_t*)(s + o_pow);
   p.tickets = (unsigned*)(s + o_tk);
   p.best_val = (float*)(s + o_bv); p.best_idx = (int*)(s + o_bi); p.best_bad = (int*)(s + o_bb);
   p.err = (int*)(s + o_err);

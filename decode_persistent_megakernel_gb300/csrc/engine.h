@@ -84,9 +84,12 @@ struct __align__(16) StepParams {
   uint64_t* act;           // [F]
   unsigned epoch;          // stamps of this launch: phase k writes epoch + k
   int stamp_check;         // readers wait for the stamp (persistent kernel); 0: stream order suffices
-  float* part_m;           // [nq][nch_cap]
+  float* part_m;           // [nq][nch_cap]      (per-phase kernels: ticket merge)
   float* part_l;           // [nq][nch_cap]
   float* part_o;           // [nq][nch_cap][d]
+  uint64_t* part_mw;       // [nq][nch_cap]      stamped copies (persistent kernel: every unit
+  uint64_t* part_lw;       // [nq][nch_cap]      merges a slice of its head's outputs)
+  uint64_t* part_ow;       // [nq][nch_cap][d]
   unsigned* tickets;       // [nkv + 1]: attention merge per KV head, then the argmax ticket
   float* best_val;         // [grid]
   int* best_idx;           // [grid]

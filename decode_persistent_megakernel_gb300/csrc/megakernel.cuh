@@ -62,6 +62,11 @@ __device__ __forceinline__ AttnArgs step_attn_args(const StepParams& p, int laye
   A.part_m = p.part_m;
   A.part_l = p.part_l;
   A.part_o = p.part_o;
+  if (p.stamp_check) {  // persistent kernel: sliced merge over stamped partials
+    A.pmw = p.part_mw;
+    A.plw = p.part_lw;
+    A.pow_ = p.part_ow;
+  }
   A.nch_cap = p.nch_cap;
   A.tickets = p.tickets;
   A.out = nullptr;
@@ -245,6 +250,10 @@ __device__ __forceinline__ bool consume_attn_phase(const StepParams& p, Pipe& pp
   for (int u = blockIdx.x; u < units; u += p.grid) {
     if (!attn_unit(pp, A, sp, u / sp.nch, u % sp.nch, tid, tr)) return false;
     tr = nullptr;
+  }
+  if (A.pmw) {  // every unit of the CTA has published its partials: now merge the slices
+    for (int u = blockIdx.x; u < units; u += p.grid)
+      if (!attn_merge_slice(pp, A, sp, u / sp.nch, u % sp.nch, tid)) return false;
   }
   return true;
 }

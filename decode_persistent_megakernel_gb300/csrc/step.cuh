@@ -848,6 +848,11 @@ struct AttnArgs {
   int check = 0;
   uint64_t* outw = nullptr;        // stamped output (the step), written with stamp_out
   unsigned stamp_out = 0;
+  // sliced merge (persistent kernel): partials as stamped words, no ticket; every unit then
+  // merges a slice of its head's outputs (attn_merge_slice)
+  uint64_t* pmw = nullptr;
+  uint64_t* plw = nullptr;
+  uint64_t* pow_ = nullptr;
   uint16_t* kc;            // this layer's K cache [nkv][max_ctx][d]
   uint16_t* vc;
   const float2* rope;      // [max_ctx][d/2]
@@ -871,68 +876,46 @@ __device__ __forceinline__ void produce_attn_unit(Pipe& pp, const AttnArgs& A, i
   prod_push(pp, A.vc + base, (uint32_t)(nk * A.d * 2), pol, dead);
 }
 
-// Merge of one KV head's chunk partials for its query heads (the log-sum-exp combine). Every
-// thread first issues the loads of its output element's chunk outputs (they do not depend on the
-// weights), warp g meanwhile finds head g's maximum and weights (lanes over chunks); then each output
-// sums its chunks in a fixed order.
+// One merged attention output (the log-sum-exp combine of a head's chunk partials for one
+// dimension): lanes over chunks, 32 at a time, combined with a running maximum. part(cc, m, l, v)
+// delivers chunk cc's max, sum and output value. Both merges (ticket and sliced) use it, so that
+// the persistent kernel and the per-phase kernels produce the same bits. Result in every lane.
+template <class Part>
+__device__ __forceinline__ float merge_one(int nch, int lane, Part part) {
+  float M = -CUDART_INF_F, num = 0.f, den = 0.f;
+  for (int cb = 0; cb < nch; cb += 32) {
+    const int cc = cb + lane;
+    float m = -CUDART_INF_F, l = 0.f, v = 0.f;
+    if (cc < nch) part(cc, m, l, v);
+    const float Mn = fmaxf(M, warp_max(m));
+    const float keep = M == -CUDART_INF_F ? 0.f : expf(M - Mn);
+    const float w = m == -CUDART_INF_F ? 0.f : expf(m - Mn);  // an empty chunk weighs exactly 0
+    num = num * keep + warp_sum(w * v);
+    den = den * keep + warp_sum(w * l);
+    M = Mn;
+  }
+  return num / den;
+}
+
+// Merge of one KV head's chunk partials for its query heads by the CTA that took the head's last
+// ticket: one warp per output.
 static __device__ void attn_merge(const AttnArgs& A, Misc* ms, int tid, int j, int nch) {
-  constexpr int MB = 32;  // chunk outputs in flight per thread
+  (void)ms;
   const int G = A.nq / A.nkv, d = A.d;
   const int warp = tid >> 5, lane = tid & 31;
-  const int nout = G * d;
-  float ob[MB];
-  const float* po0 = nullptr;
-  if (tid < nout) {
-    const int g = tid / d, i = tid - g * d;
-    po0 = A.part_o + (size_t)(j * G + g) * A.nch_cap * d + i;
-#pragma unroll
-    for (int u = 0; u < MB; ++u) ob[u] = u < nch ? __ldcg(po0 + (size_t)u * d) : 0.f;
-  }
-  if (warp < G) {
-    // head g = warp: lanes over chunks, m and l loaded once (up to 8 chunks per lane)
-    const int h = j * G + warp;
-    float mc[T_MAX / 32], lc[T_MAX / 32];
-    float M = -CUDART_INF_F;
-#pragma unroll
-    for (int k = 0; k < T_MAX / 32; ++k) {
-      const int c = lane + 32 * k;
-      mc[k] = c < nch ? __ldcg(A.part_m + (size_t)h * A.nch_cap + c) : -CUDART_INF_F;
-      lc[k] = c < nch ? __ldcg(A.part_l + (size_t)h * A.nch_cap + c) : 0.f;
-      M = fmaxf(M, mc[k]);
+  for (int o = warp; o < G * d; o += NCW) {
+    const int g = o / d, i = o - g * d, h = j * G + g;
+    const float r = merge_one(nch, lane, [&](int cc, float& m, float& l, float& v) {
+      const size_t mi = (size_t)h * A.nch_cap + cc;
+      m = __ldcg(A.part_m + mi);
+      l = __ldcg(A.part_l + mi);
+      v = __ldcg(A.part_o + mi * d + i);
+    });
+    if (lane == 0) {
+      const size_t oi = (size_t)h * d + i;
+      if (A.outw) A.outw[oi] = stamp_word(r, A.stamp_out);
+      else A.out[oi] = r;
     }
-    M = warp_max(M);
-    float den = 0.f;
-#pragma unroll
-    for (int k = 0; k < T_MAX / 32; ++k) {
-      const int c = lane + 32 * k;
-      const float w = mc[k] == -CUDART_INF_F ? 0.f : expf(mc[k] - M);  // an empty chunk weighs exactly 0
-      if (c < nch) ms->sc[warp * T_MAX + c] = w;
-      den = fmaf(w, lc[k], den);
-    }
-    den = warp_sum(den);
-    if (lane == 0) ms->hl[warp] = 1.f / den;
-  }
-  named_sync(BAR_CONS, NCT);
-  for (int idx = tid; idx < nout; idx += NCT) {
-    const int g = idx / d, i = idx - g * d;
-    const float* po = A.part_o + (size_t)(j * G + g) * A.nch_cap * d + i;
-    const float* wg = ms->sc + g * T_MAX;
-    float acc = 0.f;
-    int c = 0;
-    if (idx == tid) {  // the first batch is already loaded
-#pragma unroll
-      for (int u = 0; u < MB; ++u) acc = u < nch ? fmaf(wg[u], ob[u], acc) : acc;
-      c = MB;
-    }
-    for (; c < nch; c += MB) {
-#pragma unroll
-      for (int u = 0; u < MB; ++u) ob[u] = c + u < nch ? __ldcg(po + (size_t)(c + u) * d) : 0.f;
-#pragma unroll
-      for (int u = 0; u < MB; ++u) acc = c + u < nch ? fmaf(wg[c + u], ob[u], acc) : acc;
-    }
-    const size_t oi = (size_t)(j * G + g) * d + i;
-    if (A.outw) A.outw[oi] = stamp_word(acc * ms->hl[g], A.stamp_out);
-    else A.out[oi] = acc * ms->hl[g];
   }
 }
 
@@ -1195,17 +1178,30 @@ static __device__ bool attn_unit(Pipe& pp, const AttnArgs& A, const AttnSplit& s
       if (has_pos) o1 = fma2(make_float2(pg[nk], pg[nk]), make_float2(vn[2 * i2], vn[2 * i2 + 1]), o1);
       const float2 o = make_float2((o0.x + o1.x) + (o2.x + o3.x), (o0.y + o1.y) + (o2.y + o3.y));
       const int h = j * G + g;
-      *reinterpret_cast<float2*>(A.part_o + ((size_t)h * A.nch_cap + c) * d + 2 * i2) = o;
+      const size_t oi = ((size_t)h * A.nch_cap + c) * d + 2 * i2;
+      if (A.pow_) {
+        *reinterpret_cast<ulonglong2*>(A.pow_ + oi) =
+            make_ulonglong2(stamp_word(o.x, A.stamp_out), stamp_word(o.y, A.stamp_out));
+      } else {
+        *reinterpret_cast<float2*>(A.part_o + oi) = o;
+      }
     }
   }
   cons_release(pp, lane);
   if (tid < G) {
     const int h = j * G + tid;
-    A.part_m[(size_t)h * A.nch_cap + c] = ms->hm[tid];
-    A.part_l[(size_t)h * A.nch_cap + c] = ms->hl[tid];
+    const size_t mi = (size_t)h * A.nch_cap + c;
+    if (A.pmw) {
+      A.pmw[mi] = stamp_word(ms->hm[tid], A.stamp_out);
+      A.plw[mi] = stamp_word(ms->hl[tid], A.stamp_out);
+    } else {
+      A.part_m[mi] = ms->hm[tid];
+      A.part_l[mi] = ms->hl[tid];
+    }
   }
   named_sync(BAR_CONS, NCT);
   if (tr && tid == 0) tr[TR_FETCHED] = globaltimer();
+  if (A.pmw) return true;  // sliced merge: attn_merge_slice follows once every unit is done
   if (tid == 0) {
     // release publishes this CTA's partials (ordered before by the barrier); acquire makes the
     // other CTAs' partials visible to the merging CTA
@@ -1220,6 +1216,44 @@ static __device__ bool attn_unit(Pipe& pp, const AttnArgs& A, const AttnSplit& s
   }
   named_sync(BAR_CONS, NCT);
   return true;
+}
+
+// Sliced merge of unit (KV head j, chunk c): once the partials of every chunk of head j carry this
+// phase's stamp, the unit combines the outputs [c * per, (c + 1) * per) of the head's G * d outputs
+// (per = ceil(G * d / nch)), one warp per output, lanes over chunks, and writes them as stamped
+// words. No ticket: every unit waits only for its siblings' partials, and the whole merge is spread
+// over the head's units. Returns false (the same in every consumer thread) if partials never came.
+static __device__ bool attn_merge_slice(Pipe& pp, const AttnArgs& A, const AttnSplit& sp, int j, int c,
+                                        int tid) {
+  const int G = A.nq / A.nkv, d = A.d, nch = sp.nch;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int nout = G * d, per = (nout + nch - 1) / nch;
+  const int o0 = c * per, o1 = min(o0 + per, nout);
+  const unsigned sv = A.stamp_out;
+  const bool check = A.check != 0;
+  auto get = [&](const uint64_t* p) -> float {
+    uint64_t w = __ldcg(reinterpret_cast<const unsigned long long*>(p));
+    if (check) {
+      Poll pl;
+      while (word_stamp(w) != sv && pl.again(pp)) w = __ldcg(reinterpret_cast<const unsigned long long*>(p));
+    }
+    return word_value(w);
+  };
+  for (int o = o0 + warp; o < o1; o += NCW) {
+    const int g = o / d, i = o - g * d, h = j * G + g;
+    const float r = merge_one(nch, lane, [&](int cc, float& m, float& l, float& v) {
+      const size_t mi = (size_t)h * A.nch_cap + cc;  // the three loads first, then their stamps
+      const uint64_t wm = __ldcg(reinterpret_cast<const unsigned long long*>(A.pmw + mi));
+      const uint64_t wl = __ldcg(reinterpret_cast<const unsigned long long*>(A.plw + mi));
+      const uint64_t wo = __ldcg(reinterpret_cast<const unsigned long long*>(A.pow_ + mi * d + i));
+      m = word_stamp(wm) == sv || !check ? word_value(wm) : get(A.pmw + mi);
+      l = word_stamp(wl) == sv || !check ? word_value(wl) : get(A.plw + mi);
+      v = word_stamp(wo) == sv || !check ? word_value(wo) : get(A.pow_ + mi * d + i);
+    });
+    if (lane == 0) A.outw[(size_t)h * d + i] = stamp_word(r, A.stamp_out);
+  }
+  named_sync(BAR_CONS, NCT);
+  return !*reinterpret_cast<volatile int*>(&pp.ms->abort);
 }
 
 }  // namespace tinfer
