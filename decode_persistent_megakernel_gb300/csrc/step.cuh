@@ -407,8 +407,6 @@ __device__ __forceinline__ void best_update(Best& b, float v, int i) {
   else if (v > b.v || (v == b.v && i < b.i)) { b.v = v; b.i = i; }
 }
 
-constexpr int FETCH_IF = 4;  // 16-byte blocks a thread has in flight per turn of the vector fetch
-constexpr int GAIN_PRE = 4;  // gain blocks a thread loads ahead (vectors of up to 4 * 4 * NCT inputs)
 
 __device__ __forceinline__ float4 gain_block(const ActSrc& src, int j) {
   if (src.gf) return __ldg(reinterpret_cast<const float4*>(src.gf) + j);
@@ -416,29 +414,30 @@ __device__ __forceinline__ float4 gain_block(const ActSrc& src, int j) {
   return make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
 }
 
-// The phase's input vector, written by other CTAs before the last grid barrier, fetched once per
-// CTA into shared memory by all consumer threads together (16-byte loads through L2, thread t
-// taking blocks t, t + NCT, ...): every warp of every CTA reading the same few cache lines
-// serialises on those lines, one read per CTA does not, and the load path does not queue behind
-// the CTA's own bulk weight copies. With an RMSNorm gain the stored values are x * g (the first
-// GAIN_PRE gain blocks of the thread come from `gpre`, loaded before the barrier) and the sum of
-// squares of x is reduced on the way; the return value is 1 / rms(x) (1 without a norm), the same in
-// every consumer thread. Returns after the named barrier that publishes the copy; the CTA's abort
-// flag is then set (the same in every thread) if a stamped source never showed up.
-__device__ __forceinline__ float fetch_vector(Pipe& pp, const ActSrc& src, const float4* gpre, int tid) {
+// The phase's input vector, written by other CTAs in the previous phase, fetched once per CTA into
+// shared memory by all consumer threads together (16-byte loads through L2, thread t taking blocks
+// t, t + NCT, ...): every warp of every CTA reading the same few cache lines serialises on those
+// lines, one read per CTA does not, and the load path does not queue behind the CTA's own bulk
+// weight copies. Stamped sources are read again, block by block, until the writers' stamps show.
+// With an RMSNorm gain the stored values are x * g and the sum of squares of x is reduced on the
+// way; the return value is 1 / rms(x) (1 without a norm), the same in every consumer thread.
+// Returns after the named barrier that publishes the copy; the CTA's abort flag is then set (the
+// same in every thread) if a stamped source never showed up.
+template <int IF>
+__device__ __forceinline__ float fetch_vector_n(Pipe& pp, const ActSrc& src, int tid) {
   const bool norm = src.gf || src.gb;
   const int nb = src.n / 4;
   float4* xs = sptr_w<float4>(pp.xs);
   float ss = 0.f;
-  for (int j0 = tid, turn = 0; j0 < nb; j0 += FETCH_IF * NCT, ++turn) {
-    float4 x[FETCH_IF];
+  for (int j0 = tid; j0 < nb; j0 += IF * NCT) {
+    float4 x[IF];
     if (src.xw) {
       // two 16-byte loads per block of 4 stamped words; stale blocks are read again until their
       // writers' stamps show (bounded)
       const ulonglong2* xw = reinterpret_cast<const ulonglong2*>(src.xw);
-      ulonglong2 w0[FETCH_IF], w1[FETCH_IF];
+      ulonglong2 w0[IF], w1[IF];
 #pragma unroll
-      for (int u = 0; u < FETCH_IF; ++u) {
+      for (int u = 0; u < IF; ++u) {
         const int j = j0 + u * NCT;
         if (j < nb) {
           w0[u] = __ldcg(xw + 2 * j);
@@ -446,7 +445,7 @@ __device__ __forceinline__ float fetch_vector(Pipe& pp, const ActSrc& src, const
         }
       }
 #pragma unroll
-      for (int u = 0; u < FETCH_IF; ++u) {
+      for (int u = 0; u < IF; ++u) {
         const int j = j0 + u * NCT;
         if (j < nb) {
           if (src.check) {
@@ -466,21 +465,21 @@ __device__ __forceinline__ float fetch_vector(Pipe& pp, const ActSrc& src, const
     } else if (src.xf) {
       const float4* xf = reinterpret_cast<const float4*>(src.xf);
 #pragma unroll
-      for (int u = 0; u < FETCH_IF; ++u) {
+      for (int u = 0; u < IF; ++u) {
         const int j = j0 + u * NCT;
         x[u] = j < nb ? __ldcg(xf + j) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     } else {
       const uint2* xb = reinterpret_cast<const uint2*>(src.xb);
 #pragma unroll
-      for (int u = 0; u < FETCH_IF; ++u) {
+      for (int u = 0; u < IF; ++u) {
         const int j = j0 + u * NCT;
         const uint2 w = j < nb ? __ldg(xb + j) : make_uint2(0u, 0u);
         x[u] = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
       }
     }
 #pragma unroll
-    for (int u = 0; u < FETCH_IF; ++u) {
+    for (int u = 0; u < IF; ++u) {
       const int j = j0 + u * NCT;
       if (j < nb) {
         ss = fmaf(x[u].x, x[u].x, ss);
@@ -488,7 +487,7 @@ __device__ __forceinline__ float fetch_vector(Pipe& pp, const ActSrc& src, const
         ss = fmaf(x[u].z, x[u].z, ss);
         ss = fmaf(x[u].w, x[u].w, ss);
         float4 g = make_float4(1.f, 1.f, 1.f, 1.f);
-        if (norm) g = (gpre && turn == 0) ? gpre[u] : gain_block(src, j);
+        if (norm) g = gain_block(src, j);
         xs[j] = make_float4(x[u].x * g.x, x[u].y * g.y, x[u].z * g.z, x[u].w * g.w);
       }
     }
@@ -503,6 +502,11 @@ __device__ __forceinline__ float fetch_vector(Pipe& pp, const ActSrc& src, const
 #pragma unroll
   for (int w = 0; w < NCW; ++w) tot += pp.ms->wred[w];
   return 1.f / sqrtf(tot / (float)src.n + src.eps);
+}
+
+// Four blocks in flight per thread and turn (more would spill the persistent kernel's registers).
+__device__ __forceinline__ float fetch_vector(Pipe& pp, const ActSrc& src, int tid) {
+  return fetch_vector_n<4>(pp, src, tid);
 }
 
 // One lane's chunk of the input vector from the shared-memory copy: E / 4 consecutive 16-byte blocks
@@ -594,7 +598,7 @@ __device__ __forceinline__ bool gemv_rows(Pipe& pp, const GemvPlan& pl, Best& be
   // registers, scaled by 1 / rms(x); chunks past the segment read the segment's last chunk slot and
   // are zeroed, so that the row loop needs no per-lane branches
   if (tr_ready && tid == 0) tr_ready[TR_ENTRY - TR_READY] = globaltimer();
-  const float inv = fetch_vector(pp, src, nullptr, tid);
+  const float inv = fetch_vector(pp, src, tid);
   if (tr_ready && tid == 0) tr_ready[TR_FETCHED - TR_READY] = globaltimer();
   if (*reinterpret_cast<volatile int*>(&pp.ms->abort)) return false;  // uniform after the fetch
   (void)norm;
