@@ -894,32 +894,73 @@ __device__ __forceinline__ float merge_one(int nch, int lane, Part part) {
     const float Mn = fmaxf(M, warp_max(m));
     const float keep = M == -CUDART_INF_F ? 0.f : expf(M - Mn);
     const float w = m == -CUDART_INF_F ? 0.f : expf(m - Mn);  // an empty chunk weighs exactly 0
-    num = num * keep + warp_sum(w * v);
-    den = den * keep + warp_sum(w * l);
+    // explicit roundings (no contraction differences between the two merges)
+    num = __fmaf_rn(num, keep, warp_sum(__fmul_rn(w, v)));
+    den = __fmaf_rn(den, keep, warp_sum(__fmul_rn(w, l)));
     M = Mn;
   }
   return num / den;
 }
 
+// The sum warp_sum leaves in every lane, computed by one thread from the 32 lane values: the same
+// xor butterfly (partners 16, 8, 4, 2, 1), so the same additions in the same order, the same bits.
+__device__ __forceinline__ float butterfly_sum32(float (&v)[32]) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+#pragma unroll
+    for (int i = 0; i < o; ++i) v[i] = v[i] + v[i + o];
+  }
+  return v[0];
+}
+
 // Merge of one KV head's chunk partials for its query heads by the CTA that took the head's last
-// ticket: one warp per output.
+// ticket (per-phase kernels). Warp g computes head g's chunk weights and denominator exactly as
+// merge_one does; then one thread per output repeats merge_one's numerator with butterfly_sum32,
+// so that the result has merge_one's bits while the G * d outputs are computed in parallel.
 static __device__ void attn_merge(const AttnArgs& A, Misc* ms, int tid, int j, int nch) {
-  (void)ms;
   const int G = A.nq / A.nkv, d = A.d;
   const int warp = tid >> 5, lane = tid & 31;
-  for (int o = warp; o < G * d; o += NCW) {
-    const int g = o / d, i = o - g * d, h = j * G + g;
-    const float r = merge_one(nch, lane, [&](int cc, float& m, float& l, float& v) {
-      const size_t mi = (size_t)h * A.nch_cap + cc;
-      m = __ldcg(A.part_m + mi);
-      l = __ldcg(A.part_l + mi);
-      v = __ldcg(A.part_o + mi * d + i);
-    });
-    if (lane == 0) {
-      const size_t oi = (size_t)h * d + i;
-      if (A.outw) A.outw[oi] = stamp_word(r, A.stamp_out);
-      else A.out[oi] = r;
+  const int nb = (nch + 31) / 32;
+  float* w = ms->sc;     // [g][c] chunk weights
+  float* keep = ms->qs;  // [g][batch] rescale of the running sums
+  if (warp < G) {
+    const int h = j * G + warp;
+    float M = -CUDART_INF_F, den = 0.f;
+    for (int b = 0; b < nb; ++b) {
+      const int cc = 32 * b + lane;
+      float m = -CUDART_INF_F, l = 0.f;
+      if (cc < nch) {
+        m = __ldcg(A.part_m + (size_t)h * A.nch_cap + cc);
+        l = __ldcg(A.part_l + (size_t)h * A.nch_cap + cc);
+      }
+      const float Mn = fmaxf(M, warp_max(m));
+      const float kp = M == -CUDART_INF_F ? 0.f : expf(M - Mn);
+      const float wc = m == -CUDART_INF_F ? 0.f : expf(m - Mn);
+      if (cc < nch) w[warp * T_MAX + cc] = wc;
+      if (lane == 0) keep[warp * (T_MAX / 32) + b] = kp;
+      den = __fmaf_rn(den, kp, warp_sum(__fmul_rn(wc, l)));
+      M = Mn;
     }
+    if (lane == 0) ms->hl[warp] = den;
+  }
+  named_sync(BAR_CONS, NCT);
+  for (int o = tid; o < G * d; o += NCT) {
+    const int g = o / d, i = o - g * d, h = j * G + g;
+    const float* po = A.part_o + (size_t)h * A.nch_cap * d + i;
+    float num = 0.f;
+    for (int b = 0; b < nb; ++b) {
+      float t[32];
+#pragma unroll
+      for (int q = 0; q < 32; ++q) {
+        const int cc = 32 * b + q;
+        t[q] = cc < nch ? __fmul_rn(w[g * T_MAX + cc], __ldcg(po + (size_t)cc * d)) : 0.f;
+      }
+      num = __fmaf_rn(num, keep[g * (T_MAX / 32) + b], butterfly_sum32(t));
+    }
+    const float r = num / ms->hl[g];
+    const size_t oi = (size_t)h * d + i;
+    if (A.outw) A.outw[oi] = stamp_word(r, A.stamp_out);
+    else A.out[oi] = r;
   }
 }
 
