@@ -21,9 +21,13 @@ constexpr int NTHREADS = NCT + 32;
 // thread (its copy cursor and the L2 lookahead cursor), the consumer warps grow to REG_CONSUMER.
 // Launch total: 12 warps x 32 x 168 = 64512 = 8 x 32 x REG_CONSUMER + 4 x 32 x REG_PRODUCER.
 constexpr int NTHREADS_MEGA = NCT + 128;
-constexpr int REG_CONSUMER = 200;
-constexpr int REG_PRODUCER = 104;
+// The int4 instances carry a second GEMV (int4 linears and the bf16 LM head) and the dequantisation
+// temporaries, so their consumers take more and their producer group less.
+constexpr int REG_CONSUMER = 200, REG_CONSUMER_INT4 = 216;
+constexpr int REG_PRODUCER = 104, REG_PRODUCER_INT4 = 72;
 static_assert(NCW * 32 * REG_CONSUMER + 4 * 32 * REG_PRODUCER <= (NTHREADS_MEGA / 32) * 32 * 168,
+              "register split exceeds the launch allocation");
+static_assert(NCW * 32 * REG_CONSUMER_INT4 + 4 * 32 * REG_PRODUCER_INT4 <= (NTHREADS_MEGA / 32) * 32 * 168,
               "register split exceeds the launch allocation");
 constexpr int NR_MAX = 32;    // rows of one matrix held by one ring stage, at most
 constexpr int G_MAX = 8;      // query heads sharing one KV head, at most
@@ -127,8 +131,8 @@ enum TraceField : int {
   TR_ACT = 5,        // the phase's input activations are in registers (before the norm)
   TR_ENTRY = 6,      // the GEMV code of the phase starts (after the phase set-up)
   TR_FETCHED = 7,    // the input vector is in shared memory
-  TR_AUX0 = 8,       // attention: the first unit's values have arrived (softmax done)
-  TR_AUX1 = 9,       // attention: this CTA won a merge ticket and starts merging
+  TR_AUX0 = 8,       // GEMV: the first weight stage is in; attention: the first unit's values are in
+  TR_AUX1 = 9,       // GEMV: the last weight stage is consumed; attention: merge started
   TRACE_FIELDS = 10
 };
 

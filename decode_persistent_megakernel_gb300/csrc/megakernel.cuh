@@ -402,10 +402,10 @@ __global__ void __launch_bounds__(NTHREADS_MEGA, 1) decode_megakernel(const __gr
   const int nph = p.m.L * PHASES_PER_LAYER + 1;
   const int tid = threadIdx.x;
   if (tid >= NCT) {
-    reg_dealloc<REG_PRODUCER>();
+    reg_dealloc<FMT ? REG_PRODUCER_INT4 : REG_PRODUCER>();
     if (tid == NCT) produce_step(p, pp, pos, trace);
   } else {
-    reg_alloc<REG_CONSUMER>();
+    reg_alloc<FMT ? REG_CONSUMER_INT4 : REG_CONSUMER>();
     // no grid barrier: each phase waits, inside its input fetch, for the stamps of the results it
     // reads, so a CTA starts a phase as soon as its own inputs are complete
     fill_phase_table(p, s_tab, tid);

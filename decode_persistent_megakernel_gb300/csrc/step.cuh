@@ -676,8 +676,10 @@ __device__ __forceinline__ bool gemv_rows(Pipe& pp, const GemvPlan& pl, Best& be
   for (int s0 = rs.r0; s0 < rs.r1; s0 += rs.nr) {
     const int nrs = min(rs.nr, rs.r1 - s0);
     const uint32_t st = cons_acquire(pp);
+    if (tr_ready && tid == 0 && s0 == rs.r0) tr_ready[TR_AUX0 - TR_READY] = globaltimer();
+    int i0 = grp;
 #pragma unroll 1
-    for (int i = grp; i < nrs; i += WG) {
+    for (int i = i0; i < nrs; i += WG) {
       const uint32_t rowp = st + (uint32_t)i * g.rb;
       float2 acc = make_float2(0.f, 0.f), acc2 = make_float2(0.f, 0.f);
       // every chunk is loaded unconditionally (clamped offsets, zero activations past the row), so
@@ -705,6 +707,7 @@ __device__ __forceinline__ bool gemv_rows(Pipe& pp, const GemvPlan& pl, Best& be
     }
     cons_release(pp, lane);
   }
+  if (tr_ready && tid == 0) tr_ready[TR_AUX1 - TR_READY] = globaltimer();
   if (filled) flush();
   if (direct) return true;
   named_sync(BAR_CONS, NCT);

@@ -150,7 +150,8 @@ long long tinfer_query(const tinfer_ctx* ctx, int what);
  * last), ten uint64 %globaltimer nanosecond stamps at [(c * phases + k) * 10 + f] (0 where nothing
  * was recorded): f = 0 phase start (after the previous grid barrier), 2 phase end, 3 producer starts
  * issuing the phase's copies, 4 producer has issued them; GEMV phases: 1 activations normalised and
- * ready, 5 input activations in registers, 6 GEMV code entered, 7 input vector in shared memory;
+ * ready, 5 input activations in registers, 6 GEMV code entered, 7 input vector in shared memory,
+ * 8 first weight stage available, 9 last weight stage consumed;
  * attention phases (first unit of the CTA): 1 keys arrived, 5 queries rotated, 6 scores done,
  * 7 partials written, 8 values arrived, 9 merge started (CTAs that merge). NULL turns tracing off. */
 tinfer_status tinfer_set_trace(tinfer_ctx* ctx, void* trace_dev);
