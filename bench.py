@@ -50,14 +50,20 @@ KERNEL_SOURCES = ["megakernel.cuh", "step.cuh", "ptx.cuh", "engine.h", "kernels.
 
 
 def kernel_source_hash() -> str:
-    """sha256 over the device-code sources of the step kernels (names and contents)."""
+    """sha256 over the device-code sources of the step kernels (names and code; comments and
+    blank space do not count, so a comment edit keeps a recorded measurement valid)."""
     import hashlib
+    import re
     h = hashlib.sha256()
     d = os.path.join(ROOT, "decode_persistent_megakernel_gb300", "csrc")
     for name in KERNEL_SOURCES:
+        with open(os.path.join(d, name)) as f:
+            code = f.read()
+        code = re.sub(r"/\*.*?\*/", " ", code, flags=re.S)
+        code = re.sub(r"//[^\n]*", " ", code)
+        code = " ".join(code.split())
         h.update(name.encode())
-        with open(os.path.join(d, name), "rb") as f:
-            h.update(f.read())
+        h.update(code.encode())
     return h.hexdigest()
 
 

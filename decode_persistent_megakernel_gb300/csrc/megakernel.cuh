@@ -279,6 +279,17 @@ __device__ __forceinline__ void fill_phase_table(const StepParams& p, PhaseTable
 
 // The plan of a GEMV phase: QKV (RMSNorm prologue, bias), O (+ residual), gate/up (RMSNorm,
 // SwiGLU), down (+ residual) or the LM head (final RMSNorm, logits, argmax).
+//
+// Hand-off buffers without barriers. Phase k writes its results as stamped words with stamp
+// epoch + k; phase k + 1 reads them once they carry that stamp. A buffer is rewritten only by a
+// later phase of the same kind (qkv by the next layer's QKV, xa by the next O, act by the next
+// gate/up, xb by the next down; the attention output and partials by the next attention). A CTA
+// that rewrites buffer B in phase k' has, in its own phase k' - 1, read the complete results of
+// phase k' - 1 (or, for attention, its heads' q/k/v, whose writers had read the complete results
+// before them), and every CTA produced its part of those results only after it had read B in an
+// earlier phase. So no reader of B is still reading when B is rewritten. The residual rows a
+// GEMV adds to are this CTA's own (the same row split in O and down), written by the same thread,
+// so they need no stamp check.
 __device__ __forceinline__ GemvPlan plan_gemv(const StepParams& p, Pipe& pp, int phase, int layer,
                                               int k, int token, int tid, const PhaseTable* tab) {
   const Dims& m = p.m;
