@@ -887,6 +887,17 @@ __device__ __forceinline__ void produce_attn_unit(Pipe& pp, const AttnArgs& A, i
 // dimension): lanes over chunks, 32 at a time, combined with a running maximum. part(cc, m, l, v)
 // delivers chunk cc's max, sum and output value. Both merges (ticket and sliced) use it, so that
 // the persistent kernel and the per-phase kernels produce the same bits. Result in every lane.
+// One batch (32 chunks, lane = chunk) of the log-sum-exp combine: running maximum M, numerator and
+// denominator, with explicit roundings so that every merge computes the same bits.
+__device__ __forceinline__ void merge_step(float& M, float& num, float& den, float m, float l, float v) {
+  const float Mn = fmaxf(M, warp_max(m));
+  const float keep = M == -CUDART_INF_F ? 0.f : expf(M - Mn);
+  const float w = m == -CUDART_INF_F ? 0.f : expf(m - Mn);  // an empty chunk weighs exactly 0
+  num = __fmaf_rn(num, keep, warp_sum(__fmul_rn(w, v)));
+  den = __fmaf_rn(den, keep, warp_sum(__fmul_rn(w, l)));
+  M = Mn;
+}
+
 template <class Part>
 __device__ __forceinline__ float merge_one(int nch, int lane, Part part) {
   float M = -CUDART_INF_F, num = 0.f, den = 0.f;
@@ -894,13 +905,7 @@ __device__ __forceinline__ float merge_one(int nch, int lane, Part part) {
     const int cc = cb + lane;
     float m = -CUDART_INF_F, l = 0.f, v = 0.f;
     if (cc < nch) part(cc, m, l, v);
-    const float Mn = fmaxf(M, warp_max(m));
-    const float keep = M == -CUDART_INF_F ? 0.f : expf(M - Mn);
-    const float w = m == -CUDART_INF_F ? 0.f : expf(m - Mn);  // an empty chunk weighs exactly 0
-    // explicit roundings (no contraction differences between the two merges)
-    num = __fmaf_rn(num, keep, warp_sum(__fmul_rn(w, v)));
-    den = __fmaf_rn(den, keep, warp_sum(__fmul_rn(w, l)));
-    M = Mn;
+    merge_step(M, num, den, m, l, v);
   }
   return num / den;
 }
@@ -1287,18 +1292,40 @@ static __device__ bool attn_merge_slice(Pipe& pp, const AttnArgs& A, const AttnS
     }
     return word_value(w);
   };
-  for (int o = o0 + warp; o < o1; o += NCW) {
-    const int g = o / d, i = o - g * d, h = j * G + g;
-    const float r = merge_one(nch, lane, [&](int cc, float& m, float& l, float& v) {
-      const size_t mi = (size_t)h * A.nch_cap + cc;  // the three loads first, then their stamps
-      const uint64_t wm = __ldcg(reinterpret_cast<const unsigned long long*>(A.pmw + mi));
-      const uint64_t wl = __ldcg(reinterpret_cast<const unsigned long long*>(A.plw + mi));
-      const uint64_t wo = __ldcg(reinterpret_cast<const unsigned long long*>(A.pow_ + mi * d + i));
-      m = word_stamp(wm) == sv || !check ? word_value(wm) : get(A.pmw + mi);
-      l = word_stamp(wl) == sv || !check ? word_value(wl) : get(A.plw + mi);
-      v = word_stamp(wo) == sv || !check ? word_value(wo) : get(A.pow_ + mi * d + i);
-    });
-    if (lane == 0) A.outw[(size_t)h * d + i] = stamp_word(r, A.stamp_out);
+  auto word = [&](const uint64_t* p) -> uint64_t {
+    return __ldcg(reinterpret_cast<const unsigned long long*>(p));
+  };
+  auto val = [&](uint64_t w, const uint64_t* p) -> float {
+    return word_stamp(w) == sv || !check ? word_value(w) : get(p);
+  };
+  // two outputs per warp and pass: all six loads of a chunk batch are issued before any is used
+  for (int oa = o0 + warp; oa < o1; oa += 2 * NCW) {
+    const int ob = oa + NCW;
+    const bool hb = ob < o1;  // warp-uniform
+    const int ga = oa / d, ia = oa - ga * d, ha = j * G + ga;
+    const int gb = hb ? ob / d : ga, ib = hb ? ob - gb * d : ia, hb_ = j * G + gb;
+    float Ma = -CUDART_INF_F, na = 0.f, da = 0.f, Mb = -CUDART_INF_F, nb = 0.f, db = 0.f;
+    for (int cb = 0; cb < nch; cb += 32) {
+      const int cc = cb + lane;
+      const bool on = cc < nch;
+      const size_t mia = (size_t)ha * A.nch_cap + cc, mib = (size_t)hb_ * A.nch_cap + cc;
+      uint64_t wma = 0, wla = 0, woa = 0, wmb = 0, wlb = 0, wob = 0;
+      if (on) {
+        wma = word(A.pmw + mia); wla = word(A.plw + mia); woa = word(A.pow_ + mia * d + ia);
+        if (hb) { wmb = word(A.pmw + mib); wlb = word(A.plw + mib); wob = word(A.pow_ + mib * d + ib); }
+      }
+      float ma = -CUDART_INF_F, la = 0.f, va = 0.f, mb = -CUDART_INF_F, lb = 0.f, vb = 0.f;
+      if (on) {
+        ma = val(wma, A.pmw + mia); la = val(wla, A.plw + mia); va = val(woa, A.pow_ + mia * d + ia);
+        if (hb) { mb = val(wmb, A.pmw + mib); lb = val(wlb, A.plw + mib); vb = val(wob, A.pow_ + mib * d + ib); }
+      }
+      merge_step(Ma, na, da, ma, la, va);
+      if (hb) merge_step(Mb, nb, db, mb, lb, vb);
+    }
+    if (lane == 0) {
+      A.outw[(size_t)ha * d + ia] = stamp_word(na / da, A.stamp_out);
+      if (hb) A.outw[(size_t)hb_ * d + ib] = stamp_word(nb / db, A.stamp_out);
+    }
   }
   named_sync(BAR_CONS, NCT);
   return !*reinterpret_cast<volatile int*>(&pp.ms->abort);
