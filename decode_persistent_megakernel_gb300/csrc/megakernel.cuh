@@ -167,10 +167,11 @@ static __device__ bool cursor_next(const StepParams& p, StageCursor& c, int pos,
 __device__ __forceinline__ void produce_step(const StepParams& p, Pipe& pp, int pos,
                                              unsigned long long* trace) {
   const uint64_t pol_w = policy_evict_first(), pol_pf = policy_evict_normal();
+  // both cursors start before phase 0 with no stage left, so that their first cursor_next enters
+  // it (one inlined copy of the cursor code per cursor keeps the producer's code small)
   StageCursor cp{}, pf{};
-  cp.k = 0;
-  cursor_enter(p, cp, pos);
-  pf = cp;
+  cp.k = -1;
+  pf.k = -1;
   long long cend = 0, pend = 0;  // stream offsets: end of the current copy, end of prefetched bytes
   uint64_t next_pf = 0;
   bool dead = false;
@@ -194,21 +195,19 @@ __device__ __forceinline__ void produce_step(const StepParams& p, Pipe& pp, int 
         if (*done) { dead = true; break; }
         const uint64_t now = globaltimer();
         if (p.l2_lookahead > 0 && now >= next_pf) {
-          // prefetch the next stage the copies have not reached, within the lookahead window
-          const void* ps = nullptr;
-          uint32_t pb = 0;
-          bool have = false;
-          while (pend < cend) {  // catch up with the copy cursor without prefetching
+          // prefetch the next stage the copies have not reached, within the lookahead window;
+          // stages the copy cursor has already taken are skipped
+          while (pend < (1LL << 62) && pend - cend < p.l2_lookahead) {
+            const void* ps;
+            uint32_t pb;
             if (!cursor_next(p, pf, pos, ps, pb)) { pend = 1LL << 62; break; }
+            const long long start = pend;
             pend += pb;
-          }
-          if (pend >= cend && pend - cend < p.l2_lookahead && pend < (1LL << 62)) {
-            if (cursor_next(p, pf, pos, ps, pb)) { have = true; pend += pb; }
-            else pend = 1LL << 62;
-          }
-          if (have && pb) {
-            bulk_prefetch_l2(ps, pb, pol_pf);
-            next_pf = now + (uint64_t)pb * (uint64_t)p.l2_pace_ns_per_kb / 1024u;
+            if (start >= cend) {
+              if (pb) bulk_prefetch_l2(ps, pb, pol_pf);
+              next_pf = now + (uint64_t)pb * (uint64_t)p.l2_pace_ns_per_kb / 1024u;
+              break;
+            }
           }
         }
         if ((long long)(now - t0) > pp.timeout) {
