@@ -242,6 +242,8 @@ __device__ __forceinline__ bool consume_attn_phase(const StepParams& p, Pipe& pp
                                                    int tid, int k, unsigned long long* trace) {
   unsigned long long* tr_ready = trace_at(trace, p, k, TR_READY);
   if (tr_ready && tid == 0) *tr_ready = globaltimer();
+  // the attention scratch shares shared memory with the row results the QKV epilogue still reads
+  named_sync(BAR_CONS, NCT);
   const AttnArgs A = step_attn_args(p, layer, pos, k);
   const AttnSplit sp = attn_split(pos, A.nkv, A.d, p.grid, p.slot_bytes, p.n_chunks_override);
   const int units = A.nkv * sp.nch;

@@ -26,12 +26,18 @@ constexpr int MAX_STAGES = 8;
 struct __align__(16) Misc {
   unsigned long long full[MAX_STAGES];
   unsigned long long empty[MAX_STAGES];
-  float rowv[ROWV_MAX];        // row results (per segment) of the current GEMV phase
+  // GEMV phases and attention phases use the same scratch: a CTA's consumer warps pass a named
+  // barrier between the last read of one and the first write of the other
+  union {
+    float rowv[ROWV_MAX];      // row results (per segment) of the current GEMV phase
+    struct {
+      float qs[G_MAX * D_MAX]; // rotated, pre-scaled queries of the current attention unit
+      float sc[G_MAX * T_MAX]; // scores, then probabilities; merge weights in the merge
+      float kn[D_MAX];         // new key of this position (bf16-rounded, as float)
+      float vn[D_MAX];         // new value of this position (bf16-rounded, as float)
+    } at;
+  };
   float wred[NCW];             // block-reduction scratch
-  float qs[G_MAX * D_MAX];     // rotated, pre-scaled queries of the current attention unit
-  float sc[G_MAX * T_MAX];     // scores, then probabilities; merge weights in the merge
-  float kn[D_MAX];             // new key of this position (bf16-rounded, as float)
-  float vn[D_MAX];             // new value of this position (bf16-rounded, as float)
   float hm[G_MAX];
   float hl[G_MAX];
   float bv[NCW];
@@ -929,8 +935,8 @@ static __device__ void attn_merge(const AttnArgs& A, Misc* ms, int tid, int j, i
   const int G = A.nq / A.nkv, d = A.d;
   const int warp = tid >> 5, lane = tid & 31;
   const int nb = (nch + 31) / 32;
-  float* w = ms->sc;     // [g][c] chunk weights
-  float* keep = ms->qs;  // [g][batch] rescale of the running sums
+  float* w = ms->at.sc;     // [g][c] chunk weights
+  float* keep = ms->at.qs;  // [g][batch] rescale of the running sums
   if (warp < G) {
     const int h = j * G + warp;
     float M = -CUDART_INF_F, den = 0.f;
@@ -1118,10 +1124,10 @@ static __device__ bool attn_unit(Pipe& pp, const AttnArgs& A, const AttnSplit& s
     }
     return word_value(w);
   };
-  float* qs = sptr_w<float>(smem_addr(ms->qs));
-  float* sc = sptr_w<float>(smem_addr(ms->sc));
-  float* kn = sptr_w<float>(smem_addr(ms->kn));
-  float* vn = sptr_w<float>(smem_addr(ms->vn));
+  float* qs = sptr_w<float>(smem_addr(ms->at.qs));
+  float* sc = sptr_w<float>(smem_addr(ms->at.sc));
+  float* kn = sptr_w<float>(smem_addr(ms->at.kn));
+  float* vn = sptr_w<float>(smem_addr(ms->at.vn));
 
   constexpr int QR = (G_MAX * D_MAX / 2 + NCT - 1) / NCT;  // query pairs per thread, at most
   uint64_t wq[QR][2];
