@@ -434,14 +434,17 @@ tinfer_status tinfer_create(const tinfer_config* c, const tinfer_weights* w, voi
   p.grid = grid;
   p.slot_bytes = x->slot;
   p.inflight = 2;
+  p.inflight_lm = 4;
   p.l2_lookahead = 512 * 1024;
   p.l2_pace_ns_per_kb = 24;
   {
     // tuning overrides for experiments: TINFER_L2_LOOKAHEAD (bytes per CTA, 0 = off),
-    // TINFER_L2_PACE (ns per KB), TINFER_INFLIGHT (bulk copies outstanding)
+    // TINFER_L2_PACE (ns per KB), TINFER_INFLIGHT / TINFER_INFLIGHT_LM (bulk copies outstanding,
+    // below ring_stages)
     if (const char* e = getenv("TINFER_L2_LOOKAHEAD")) p.l2_lookahead = atoi(e);
     if (const char* e = getenv("TINFER_L2_PACE")) p.l2_pace_ns_per_kb = atoi(e);
     if (const char* e = getenv("TINFER_INFLIGHT")) p.inflight = atoi(e);
+    if (const char* e = getenv("TINFER_INFLIGHT_LM")) p.inflight_lm = atoi(e);
   }
   p.timeout_ns = DEFAULT_TIMEOUT_NS;
   p.step_dev = (int*)(s + o_step);

@@ -105,6 +105,7 @@ struct __align__(16) StepParams {
   int ring_stages;
   int slot_bytes;
   int inflight;            // bulk copies the producer keeps outstanding at most
+  int inflight_lm;         // the same during the LM head, which streams from HBM with nothing to overlap
   int l2_lookahead;        // persistent kernel: bytes per CTA prefetched into L2 ahead of the ring
   int l2_pace_ns_per_kb;   // spacing of those prefetches (about the per-SM share of HBM bandwidth)
   long long timeout_ns;

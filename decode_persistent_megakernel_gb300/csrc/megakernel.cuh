@@ -159,7 +159,7 @@ static __device__ bool cursor_next(const StepParams& p, StageCursor& c, int pos,
 }
 
 // The persistent kernel's producer: feeds the ring in schedule order with bulk copies (at most
-// p.inflight outstanding). While the ring is full -- the consumers are in a latency-bound stretch
+// p.inflight outstanding, p.inflight_lm during the LM head). While the ring is full -- the consumers are in a latency-bound stretch
 // (barrier, attention, a small matrix) -- it walks a second cursor ahead and prefetches upcoming
 // stages into L2, paced at about this SM's share of HBM bandwidth and at most l2_lookahead bytes
 // beyond the copies, so that HBM keeps streaming while the ring cannot take more. Later copies of
@@ -179,6 +179,7 @@ __device__ __forceinline__ void produce_step(const StepParams& p, Pipe& pp, int 
   uint32_t bytes;
   const volatile int* done = &pp.ms->cons_done;
   int last_k = -1;
+  const int nph = p.m.L * PHASES_PER_LAYER + 1;
   while (!dead && cursor_next(p, cp, pos, src, bytes)) {
     if (trace && cp.k != last_k) {  // timeline: the producer moves on to phase cp.k
       const uint64_t t = globaltimer();
@@ -218,8 +219,9 @@ __device__ __forceinline__ void produce_step(const StepParams& p, Pipe& pp, int 
       }
       if (dead) break;
     }
-    if (pp.inflight > 0 && pp.it >= (uint32_t)pp.inflight) {
-      const int k = pp.inflight;
+    const int infl = min(cp.k == nph - 1 ? p.inflight_lm : pp.inflight, pp.stages);  // <= ring
+    if (infl > 0 && pp.it >= (uint32_t)infl) {
+      const int k = infl;
       const int s2 = s >= k ? s - k : s - k + pp.stages;
       const uint32_t p2 = s >= k ? pp.ph : pp.ph ^ 1u;
       if (!mbar_try_wait(pp.full0 + 8u * s2, p2) &&

@@ -601,8 +601,9 @@ __device__ __forceinline__ bool gemv_rows(Pipe& pp, const GemvPlan& pl, Best& be
   }
 
   // the input vector (x * g for RMSNorm phases) into shared memory, then this warp's segment into
-  // registers, scaled by 1 / rms(x); chunks past the segment read the segment's last chunk slot and
-  // are zeroed, so that the row loop needs no per-lane branches
+  // registers; 1 / rms(x) scales each row segment's sum instead (once per row, not per input).
+  // Chunks past the segment read the segment's last chunk slot and are zeroed, so that the row loop
+  // needs no per-lane branches
   if (tr_ready && tid == 0) tr_ready[TR_ENTRY - TR_READY] = globaltimer();
   const float inv = fetch_vector(pp, src, tid);
   if (tr_ready && tid == 0) tr_ready[TR_FETCHED - TR_READY] = globaltimer();
@@ -620,10 +621,10 @@ __device__ __forceinline__ bool gemv_rows(Pipe& pp, const GemvPlan& pl, Best& be
       load_chunk<E>(xsv, (seg * si.ks + c * E) / 4, lane, v);
 #pragma unroll
       for (int b = 0; b < E / 4; ++b) {
-        a[k][4 * b + 0] = ok ? v[b].x * inv : 0.f;
-        a[k][4 * b + 1] = ok ? v[b].y * inv : 0.f;
-        a[k][4 * b + 2] = ok ? v[b].z * inv : 0.f;
-        a[k][4 * b + 3] = ok ? v[b].w * inv : 0.f;
+        a[k][4 * b + 0] = ok ? v[b].x : 0.f;
+        a[k][4 * b + 1] = ok ? v[b].y : 0.f;
+        a[k][4 * b + 2] = ok ? v[b].z : 0.f;
+        a[k][4 * b + 3] = ok ? v[b].w : 0.f;
       }
     }
   }
@@ -663,7 +664,7 @@ __device__ __forceinline__ bool gemv_rows(Pipe& pp, const GemvPlan& pl, Best& be
   int nrow = 0, filled = 0;
   auto flush = [&]() {
     const float part[8] = {w0, w1, w2, w3, w4, w5, w6, w7};
-    const float v = transpose_reduce8(part, lane);
+    const float v = transpose_reduce8(part, lane) * inv;  // the RMSNorm scale, once per row segment
     const int q8 = transpose_row8(lane);
     if ((lane & 3) == 0 && q8 < filled) {
       const int n = nrow - 1 - q8;  // slot q holds the warp's row nrow - 1 - q
