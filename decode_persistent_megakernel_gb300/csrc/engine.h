@@ -155,25 +155,24 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 
 constexpr int SEG_MAX_INPUTS = 2048;  // inputs of one row segment (activations held per lane: 64)
-constexpr int SEG_TARGET_BF16 = 1024; // bf16 rows are cut into segments of at most this, while
-                                      // fewer than NCW segments allow it
 constexpr int ROWV_MAX = 4096;        // row results of one phase kept in shared memory per CTA
 
 // GEMV row segmenting: a row of `cols` inputs is cut into nseg (a power of two, at most NCW)
 // contiguous segments of ks inputs, chs 16-byte chunks each. A warp owns one segment of a row; the
 // activations of that segment stay in its lanes' registers (chunk c = lane + 32 k). bf16 rows are
-// cut into segments of about 1024 inputs: every warp then takes two segments of each 8-row ring
-// stage (or of each 2-row stage of 8192-input rows) instead of one whole row, which halves the
-// stage hand-offs per byte and the activation registers; int4 rows keep up to 2048 inputs, which
-// is what fills their lanes' two chunks.
+// halved while their segments hold 2048 inputs or more, so that a 2048-input row becomes two
+// 1024-input segments: every warp then takes two segments of each 8-row ring stage instead of one
+// whole row, which halves the stage hand-offs per byte and the activation registers, while rows of
+// 1024-2047 inputs stay whole (each lane keeps at least four chunks). int4 rows keep up to 2048
+// inputs, which is what fills their lanes' two chunks.
 struct SegInfo {
   int nseg, ks, chs;
 };
 TINFER_HD inline SegInfo seg_info(int fmt, int cols) {
   const int E = fmt ? 32 : 8;
-  const int target = fmt ? SEG_MAX_INPUTS : SEG_TARGET_BF16;
   int nseg = 1;
-  while (cols / nseg > target && nseg < NCW) nseg *= 2;
+  while (nseg < NCW && (cols / nseg > SEG_MAX_INPUTS || (fmt == 0 && cols / nseg >= SEG_MAX_INPUTS)))
+    nseg *= 2;
   return SegInfo{nseg, cols / nseg, cols / nseg / E};
 }
 // True when the segmenting covers the row exactly and fits the per-lane register budget.
