@@ -890,10 +890,6 @@ __device__ __forceinline__ void produce_attn_unit(Pipe& pp, const AttnArgs& A, i
   prod_push(pp, A.vc + base, (uint32_t)(nk * A.d * 2), pol, dead);
 }
 
-// One merged attention output (the log-sum-exp combine of a head's chunk partials for one
-// dimension): lanes over chunks, 32 at a time, combined with a running maximum. part(cc, m, l, v)
-// delivers chunk cc's max, sum and output value. Both merges (ticket and sliced) use it, so that
-// the persistent kernel and the per-phase kernels produce the same bits. Result in every lane.
 // One batch (32 chunks, lane = chunk) of the log-sum-exp combine: running maximum M, numerator and
 // denominator, with explicit roundings so that every merge computes the same bits.
 __device__ __forceinline__ void merge_step(float& M, float& num, float& den, float m, float l, float v) {
@@ -905,6 +901,10 @@ __device__ __forceinline__ void merge_step(float& M, float& num, float& den, flo
   M = Mn;
 }
 
+// One merged attention output (the log-sum-exp combine of a head's chunk partials for one
+// dimension): lanes over chunks, 32 at a time, combined with a running maximum. part(cc, m, l, v)
+// delivers chunk cc's max, sum and output value. Both merges (ticket and sliced) follow it, so that
+// the persistent kernel and the per-phase kernels produce the same bits. Result in every lane.
 template <class Part>
 __device__ __forceinline__ float merge_one(int nch, int lane, Part part) {
   float M = -CUDART_INF_F, num = 0.f, den = 0.f;
