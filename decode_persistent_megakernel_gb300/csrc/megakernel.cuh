@@ -255,8 +255,11 @@ __device__ __forceinline__ bool consume_attn_phase(const StepParams& p, Pipe& pp
     tr = nullptr;
   }
   if (A.pmw) {  // every unit of the CTA has published its partials: now merge the slices
-    for (int u = blockIdx.x; u < units; u += p.grid)
-      if (!attn_merge_slice(pp, A, sp, u / sp.nch, u % sp.nch, tid)) return false;
+    unsigned long long* trm = trace_at(trace, p, k, 0);
+    for (int u = blockIdx.x; u < units; u += p.grid) {
+      if (!attn_merge_slice(pp, A, sp, u / sp.nch, u % sp.nch, tid, trm)) return false;
+      trm = nullptr;
+    }
   }
   return true;
 }

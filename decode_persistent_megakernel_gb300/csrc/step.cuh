@@ -319,6 +319,22 @@ __device__ __forceinline__ float2 dot8_bf16(const uint4 w, const float* a, float
   return acc;
 }
 
+// A 32-bit register holding `v` that the compiler cannot fold into an instruction's immediate.
+__device__ __forceinline__ uint32_t opaque_u32(uint32_t v) {
+  uint32_t r;
+  asm volatile("mov.b32 %0, %1;" : "=r"(r) : "r"(v));
+  return r;
+}
+
+// (x & MASK) | m in one logic instruction: the mask is the immediate, m a register. Written out
+// because a mask and a magic number that are both literals need two instructions.
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t and_or(uint32_t x, uint32_t m) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(x), "n"(MASK), "r"(m));
+  return d;
+}
+
 // 32 int4 weights (one 16-byte chunk) dotted with 32 activations, returning sum_k q_k * a_k with
 // q_k in [0, 15] (the zero point is applied by the caller). Dequantisation uses the exponent trick
 // of tinyinfer ("v0.1": OR the nibble into the mantissa of 2^23 and subtract), generalised so that
@@ -326,18 +342,18 @@ __device__ __forceinline__ float2 dot8_bf16(const uint4 w, const float* a, float
 // 2^23 + q * 16^i exactly, and the activation of that element is stored pre-multiplied by 16^-i
 // (exact, a power of two). (f - 2^23) * a' then equals q * a exactly before rounding, so each
 // product is rounded exactly as q * a would be. Pairs go through Blackwell's packed f32x2 units.
-__device__ __forceinline__ float dot32_int4(const uint4 w, const float* a) {
-  constexpr uint32_t MAG = 0x4B000000u;
+// mag holds 0x4B000000 (the bits of 2^23) in a register: one logic instruction per nibble.
+__device__ __forceinline__ float dot32_int4(const uint4 w, const float* a, uint32_t mag) {
   const float2 B = make_float2(-8388608.f, -8388608.f);
   float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
   const uint32_t words[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const uint32_t lo = words[k], hi = words[k] >> 16;
-    const float2 f01 = make_float2(__uint_as_float((lo & 0x000Fu) | MAG), __uint_as_float((lo & 0x00F0u) | MAG));
-    const float2 f23 = make_float2(__uint_as_float((lo & 0x0F00u) | MAG), __uint_as_float((lo & 0xF000u) | MAG));
-    const float2 f45 = make_float2(__uint_as_float((hi & 0x000Fu) | MAG), __uint_as_float((hi & 0x00F0u) | MAG));
-    const float2 f67 = make_float2(__uint_as_float((hi & 0x0F00u) | MAG), __uint_as_float((hi & 0xF000u) | MAG));
+    const float2 f01 = make_float2(__uint_as_float(and_or<0x000Fu>(lo, mag)), __uint_as_float(and_or<0x00F0u>(lo, mag)));
+    const float2 f23 = make_float2(__uint_as_float(and_or<0x0F00u>(lo, mag)), __uint_as_float(and_or<0xF000u>(lo, mag)));
+    const float2 f45 = make_float2(__uint_as_float(and_or<0x000Fu>(hi, mag)), __uint_as_float(and_or<0x00F0u>(hi, mag)));
+    const float2 f67 = make_float2(__uint_as_float(and_or<0x0F00u>(hi, mag)), __uint_as_float(and_or<0xF000u>(hi, mag)));
     acc0 = fma2(add2(f01, B), make_float2(a[8 * k + 0], a[8 * k + 1]), acc0);
     acc1 = fma2(add2(f23, B), make_float2(a[8 * k + 2], a[8 * k + 3]), acc1);
     acc0 = fma2(add2(f45, B), make_float2(a[8 * k + 4], a[8 * k + 5]), acc0);
@@ -644,6 +660,7 @@ __device__ __forceinline__ bool gemv_rows(Pipe& pp, const GemvPlan& pl, Best& be
   if (tr_ready && tid == 0) *tr_ready = globaltimer();
 
   const uint32_t seg_off = FMT == 0 ? (uint32_t)(seg * si.ks * 2) : (uint32_t)(seg * si.ks / 2);
+  const uint32_t mag = opaque_u32(0x4B000000u);  // int4 exponent-trick magic, kept in a register
   const uint32_t scale_off = (uint32_t)(g.cols / 2);
   // byte offsets inside a row of this lane's chunks (chunk k = lane + 32 k, clamped) and scales
   uint32_t coff[NCHL], soff[NCHL];
@@ -700,7 +717,7 @@ __device__ __forceinline__ bool gemv_rows(Pipe& pp, const GemvPlan& pl, Best& be
           if (k & 1) acc2 = dot8_bf16(wv[k], a[k], acc2);
           else acc = dot8_bf16(wv[k], a[k], acc);
         } else {
-          const float dq = dot32_int4(wv[k], a[k]);
+          const float dq = dot32_int4(wv[k], a[k], mag);
           const uint16_t sb = lds16(rowp + soff[k]);
           const float sc = g.scale_bf16 ? bf16_to_f(sb) : __half2float(__ushort_as_half(sb));
           acc.x = fmaf(sc, dq - 8.f * S[k], acc.x);
@@ -1284,7 +1301,7 @@ static __device__ bool attn_unit(Pipe& pp, const AttnArgs& A, const AttnSplit& s
 // words. No ticket: every unit waits only for its siblings' partials, and the whole merge is spread
 // over the head's units. Returns false (the same in every consumer thread) if partials never came.
 static __device__ bool attn_merge_slice(Pipe& pp, const AttnArgs& A, const AttnSplit& sp, int j, int c,
-                                        int tid) {
+                                        int tid, unsigned long long* tr = nullptr) {
   const int G = A.nq / A.nkv, d = A.d, nch = sp.nch;
   const int lane = tid & 31, warp = tid >> 5;
   const int nout = G * d, per = (nout + nch - 1) / nch;
@@ -1326,6 +1343,7 @@ static __device__ bool attn_merge_slice(Pipe& pp, const AttnArgs& A, const AttnS
         ma = val(wma, A.pmw + mia); la = val(wla, A.plw + mia); va = val(woa, A.pow_ + mia * d + ia);
         if (hb) { mb = val(wmb, A.pmw + mib); lb = val(wlb, A.plw + mib); vb = val(wob, A.pow_ + mib * d + ib); }
       }
+      if (tr && tid == 0 && cb == 0 && oa == o0) tr[TR_AUX1] = globaltimer();  // siblings' partials seen
       merge_step(Ma, na, da, ma, la, va);
       if (hb) merge_step(Mb, nb, db, mb, lb, vb);
     }
