@@ -20,6 +20,7 @@ TINFER_MEGAKERNEL, TINFER_GRAPH = 0, 1
 TINFER_Q_GRID, TINFER_Q_SMEM, TINFER_Q_RING_STAGES, TINFER_Q_SLOT_BYTES, TINFER_Q_KERNELS_PER_STEP, \
     TINFER_Q_TRACE_BYTES, TINFER_Q_BLOCK_THREADS = range(7)
 TINFER_EPI_STORE, TINFER_EPI_RESIDUAL, TINFER_EPI_SWIGLU, TINFER_EPI_ARGMAX = range(4)
+TINFER_S_INFLIGHT, TINFER_S_INFLIGHT_LM, TINFER_S_L2_LOOKAHEAD, TINFER_S_L2_PACE = range(4)
 TINFER_NOALLOC_SCRATCH_BYTES = 1 << 20
 TRACE_FIELDS = 10  # stamps per CTA and phase of the timeline (tinfer_set_trace)
 
@@ -27,8 +28,9 @@ EXPORTS = [
     "tinfer_status_string", "tinfer_check_config", "tinfer_packed_layer_bytes", "tinfer_pack_layer",
     "tinfer_unpack_layer", "tinfer_create", "tinfer_decode_step", "tinfer_decode_step_dev",
     "tinfer_generate", "tinfer_get_error", "tinfer_query", "tinfer_set_trace", "tinfer_set_timeout_ns",
-    "tinfer_debug_skip_barrier", "tinfer_destroy", "tinfer_packed_row_bytes", "tinfer_pack_matrix",
-    "tinfer_op_gemv", "tinfer_op_attention", "tinfer_op_attention_noalloc",
+    "tinfer_debug_withhold_results", "tinfer_set_schedule", "tinfer_get_schedule", "tinfer_destroy",
+    "tinfer_packed_row_bytes", "tinfer_pack_matrix", "tinfer_op_gemv", "tinfer_op_attention",
+    "tinfer_op_attention_noalloc",
 ]
 
 
@@ -88,7 +90,9 @@ def lib():
             "tinfer_query": ([P, I], LL),
             "tinfer_set_trace": ([P, P], I),
             "tinfer_set_timeout_ns": ([P, LL], I),
-            "tinfer_debug_skip_barrier": ([P, I, I], I),
+            "tinfer_debug_withhold_results": ([P, I, I], I),
+            "tinfer_set_schedule": ([P, I, LL], I),
+            "tinfer_get_schedule": ([P, I], LL),
             "tinfer_destroy": ([P], None),
             "tinfer_packed_row_bytes": ([I, I, I], Z),
             "tinfer_pack_matrix": ([I, I, I, I, I, P, P, P, P], I),
@@ -189,8 +193,16 @@ def tinfer_set_timeout_ns(ctx, ns: int) -> int:
     return lib().tinfer_set_timeout_ns(ctx, int(ns))
 
 
-def tinfer_debug_skip_barrier(ctx, cta: int, barrier: int) -> int:
-    return lib().tinfer_debug_skip_barrier(ctx, int(cta), int(barrier))
+def tinfer_debug_withhold_results(ctx, cta: int, phase: int) -> int:
+    return lib().tinfer_debug_withhold_results(ctx, int(cta), int(phase))
+
+
+def tinfer_set_schedule(ctx, knob: int, value: int) -> int:
+    return lib().tinfer_set_schedule(ctx, int(knob), int(value))
+
+
+def tinfer_get_schedule(ctx, knob: int) -> int:
+    return lib().tinfer_get_schedule(ctx, int(knob))
 
 
 def tinfer_destroy(ctx) -> None:

@@ -29,6 +29,7 @@ static_assert(NCW * 32 * REG_CONSUMER + 4 * 32 * REG_PRODUCER <= (NTHREADS_MEGA 
               "register split exceeds the launch allocation");
 static_assert(NCW * 32 * REG_CONSUMER_INT4 + 4 * 32 * REG_PRODUCER_INT4 <= (NTHREADS_MEGA / 32) * 32 * 168,
               "register split exceeds the launch allocation");
+constexpr int MAX_STAGES = 8;  // ring stages of the shared-memory weight ring, at most
 constexpr int NR_MAX = 32;    // rows of one matrix held by one ring stage, at most
 constexpr int G_MAX = 8;      // query heads sharing one KV head, at most
 constexpr int D_MAX = 128;    // head_dim, at most
@@ -118,7 +119,7 @@ struct __align__(16) StepParams {
   float* logits;           // [V] or null
   int* argmax;             // [1]
   int dbg_skip_cta;        // fault injection: CTA that withholds its results of one GEMV phase (-1 none)
-  int dbg_skip_barrier;    // ... the phase index
+  int dbg_skip_phase;    // ... the phase index
   unsigned long long* trace;  // optional timeline [grid][phases][TRACE_FIELDS] of %globaltimer ns
 };
 

@@ -1,8 +1,9 @@
 // kernels.cu -- the kernels of the engine and their launch wrappers.
 //
 // The step kernels themselves are in megakernel.cuh (instantiated by mega_bf16.cu, mega_int4.cu):
-//   decode_megakernel    one cooperative launch per step: every phase of every layer, grid
-//                        barriers between dependent phases, the weight stream running ahead of them
+//   decode_megakernel    one cooperative launch per step: every phase of every layer; each phase
+//                        waits for the stamped results of the one before it (no grid barrier), the
+//                        weight stream running ahead of them
 //   decode_phase_kernel  one phase of one layer; the CUDA-graph path chains 5 L + 1 of them with
 //                        programmatic dependent launch so that the next kernel's weight prefetch
 //                        starts while the current one finishes
@@ -50,7 +51,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) op_gemv_kernel(const __grid_const
     pl.src = ActSrc{};
     pl.src.xf = q.x; pl.src.gf = q.gain; pl.src.eps = q.eps; pl.src.n = q.cols;
     pl.epi = Epi{q.epi, q.y, q.bias, nullptr, 0u, 0};
-    gemv_plan_finish(pp, pl, tid);
     Best best{-CUDART_INF_F, 0x7FFFFFFF, 0};
     gemv_consume_any(pp, pl, best, tid, nullptr);
     if (q.epi == EK_ARGMAX) {
@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) op_attention_kernel(const __grid_
   pipe_setup(pp);
   __syncthreads();
   AttnArgs A;
-  A.qkv = q.qkv; A.kc = q.kc; A.vc = q.vc; A.rope = q.rope;
+  A.qkv = q.qkv; A.kc = q.kc; A.vc = q.vc; A.rope = q.rope; A.rope_pos0 = q.rope_pos0;
   A.part_m = q.part_m; A.part_l = q.part_l; A.part_o = q.part_o; A.nch_cap = q.nch_cap;
   A.tickets = q.tickets; A.out = q.out;
   A.nq = q.nq; A.nkv = q.nkv; A.d = q.d; A.max_ctx = q.max_ctx; A.pos = q.pos;

@@ -31,6 +31,7 @@ struct OpAttnParams {
   uint16_t* kc;
   uint16_t* vc;
   const float2* rope;
+  int rope_pos0;  // position of the table's first row (0: the full table)
   float* part_m;
   float* part_l;
   float* part_o;

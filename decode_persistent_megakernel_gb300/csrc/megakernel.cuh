@@ -296,6 +296,18 @@ __device__ __forceinline__ void fill_phase_table(const StepParams& p, PhaseTable
 // earlier phase. So no reader of B is still reading when B is rewritten. The residual rows a
 // GEMV adds to are this CTA's own (the same row split in O and down), written by the same thread,
 // so they need no stamp check.
+//
+// In memory-model terms: every stamped word is stored with a relaxed gpu-scope 64-bit store and
+// polled with relaxed gpu-scope loads (ptx.cuh). Those accesses are morally strong, so a poll that
+// races with the store is not a data race, and a 64-bit access is single-copy atomic, so a reader
+// that sees the stamp it waits for sees the value stored with it; the value needs no further
+// ordering because it travels in the same word. Write-after-read safety of a rewritten buffer rests
+// on the chain above: a CTA's results are computed from the values it loaded, so its loads of B
+// complete before it stores anything derived from them, and every rewrite of B depends, through at
+// least one complete phase of such results, on those stores. The PTX model alone does not order a
+// relaxed load before a later relaxed store to another address (a fence per thread and phase would,
+// at about the cost of the grid barrier this hand-off replaces); the data dependency through the
+// stored values is what orders them.
 __device__ __forceinline__ GemvPlan plan_gemv(const StepParams& p, Pipe& pp, int phase, int layer,
                                               int k, int token, int tid, const PhaseTable* tab) {
   const Dims& m = p.m;
@@ -341,13 +353,12 @@ __device__ __forceinline__ GemvPlan plan_gemv(const StepParams& p, Pipe& pp, int
       pl.epi = Epi{EK_ARGMAX, p.logits, nullptr, nullptr, own, 0};
       break;
   }
-  if (p.dbg_skip_cta == (int)blockIdx.x && p.dbg_skip_barrier == k) pl.epi.flags |= EF_WITHHOLD;
-  gemv_plan_finish(pp, pl, tid);
+  if (p.dbg_skip_cta == (int)blockIdx.x && p.dbg_skip_phase == k) pl.epi.flags |= EF_WITHHOLD;
   return pl;
 }
 
 // Consumer side of one GEMV phase from its plan; false when its input never showed up.
-template <int FMT, int NCHL>
+template <int FMT, int NCHL, int IF>
 __device__ __forceinline__ bool run_gemv_phase(const StepParams& p, Pipe& pp, const GemvPlan& pl,
                                                int phase, int tid, int k, unsigned long long* trace) {
   const Dims& m = p.m;
@@ -355,7 +366,7 @@ __device__ __forceinline__ bool run_gemv_phase(const StepParams& p, Pipe& pp, co
   Best best{-CUDART_INF_F, 0x7FFFFFFF, 0};
   // int4 models stream their linears as int4 and the LM head as bf16; bf16 models need one format
   const bool ok = (FMT == 1 && pl.g.fmt == 1) ? gemv_rows<1, 2>(pp, pl, best, tid, tr_ready)
-                                              : gemv_rows<0, NCHL>(pp, pl, best, tid, tr_ready);
+                                              : gemv_rows<0, NCHL, IF>(pp, pl, best, tid, tr_ready);
   if (!ok) return false;
   if (phase == PH_LM) {
     const Best cb = best_block_reduce(best, pp.ms, tid);
@@ -374,14 +385,14 @@ __device__ __forceinline__ GemvPlan plan_phase(const StepParams& p, Pipe& pp, in
   return plan_gemv(p, pp, phase, layer, k, token, tid, tab);
 }
 
-template <int FMT, int NCHL>
+template <int FMT, int NCHL, int IF>
 __device__ __forceinline__ bool run_phase(const StepParams& p, Pipe& pp, const GemvPlan& pl, int k,
                                           int token, int pos, int tid, unsigned long long* trace) {
   (void)token;
   int phase, layer;
   phase_of(k, p.m.L, phase, layer);
   if (phase == PH_ATTN) return consume_attn_phase(p, pp, layer, pos, tid, k, trace);
-  return run_gemv_phase<FMT, NCHL>(p, pp, pl, phase, tid, k, trace);
+  return run_gemv_phase<FMT, NCHL, IF>(p, pp, pl, phase, tid, k, trace);
 }
 
 // Start-of-step decision, identical in every CTA: skip when an earlier step left an error, or when
@@ -430,7 +441,7 @@ __global__ void __launch_bounds__(NTHREADS_MEGA, 1) decode_megakernel(const __gr
     for (int k = 0; k < nph; ++k) {
       if (unsigned long long* t = trace_at(trace, p, k, TR_START)) if (tid == 0) *t = globaltimer();
       const GemvPlan plan = plan_phase(p, pp, k, token, tid, &s_tab);
-      const bool ok = run_phase<FMT, NCHL>(p, pp, plan, k, token, pos, tid, trace);
+      const bool ok = run_phase<FMT, NCHL, 4>(p, pp, plan, k, token, pos, tid, trace);
       if (unsigned long long* t = trace_at(trace, p, k, TR_END)) if (tid == 0) *t = globaltimer();
       if (!ok) break;
     }
@@ -467,7 +478,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) decode_phase_kernel(const __grid_
     if (!*reinterpret_cast<volatile int*>(&pp.ms->exit_now)) {
       const int token = p.step_dev[0], pos = p.step_dev[1];
       const GemvPlan plan = plan_phase(p, pp, k, token, tid);  // after the wait: reads x of the previous kernel
-      (void)run_phase<FMT, NCHL>(p, pp, plan, k, token, pos, tid, p.trace);
+      (void)run_phase<FMT, NCHL, 4>(p, pp, plan, k, token, pos, tid, p.trace);
     }
     named_sync(BAR_CONS, NCT);
     if (tid == 0) *reinterpret_cast<volatile int*>(&pp.ms->cons_done) = 1;

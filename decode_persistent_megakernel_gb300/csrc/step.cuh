@@ -6,8 +6,9 @@
 // bytes from HBM into a ring of shared-memory slots with bulk asynchronous copies that complete on
 // per-slot mbarriers. Weights and cached K/V never depend on the current token ("Decoding in tiles",
 // section 1: the next kernel cannot start loading its weights although the weights never depend on
-// the token), so the producer runs ahead across phase boundaries and grid barriers, bounded only by
-// the ring; the consumers wait for the data dependency (a grid barrier) and then drain the slots.
+// the token), so the producer runs ahead across phase boundaries, bounded only by the ring; the
+// consumers wait for the data dependency (the stamped results of the previous phase, or stream
+// order between the per-phase kernels) and then drain the slots.
 // This is the cross-phase weight prefetch of Hazy Research's megakernel as summarised in "Decoding
 // in tiles" (section 1 and section 4), built on Blackwell's bulk-copy engine instead of per-thread
 // loads.
@@ -20,8 +21,6 @@
 #include "ptx.cuh"
 
 namespace tinfer {
-
-constexpr int MAX_STAGES = 8;
 
 struct __align__(16) Misc {
   unsigned long long full[MAX_STAGES];
@@ -137,9 +136,9 @@ __device__ __forceinline__ void prod_push(Pipe& pp, const void* src, uint32_t by
       raise_error(pp.err, pp.err_host, EW_TIMEOUT);
     return;
   }
-  if (pp.inflight > 0 && pp.it >= (uint32_t)pp.inflight) {
-    // bound the bytes in flight: the copy issued `inflight` stages ago must have landed
-    const int k = pp.inflight;
+  const int k = pp.inflight < pp.stages ? pp.inflight : pp.stages;  // never beyond the ring
+  if (k > 0 && pp.it >= (uint32_t)k) {
+    // bound the bytes in flight: the copy issued `k` stages ago must have landed
     const int s2 = s >= k ? s - k : s - k + pp.stages;
     const uint32_t p2 = s >= k ? pp.ph : pp.ph ^ 1u;
     if (!mbar_try_wait(pp.full0 + 8u * s2, p2) &&
@@ -246,16 +245,6 @@ struct Poll {
     return true;
   }
 };
-
-// The value of a stamped word once it carries `stamp` (with check; else as read).
-__device__ __forceinline__ float await_word(const uint64_t* p, unsigned stamp, bool check, const Pipe& pp) {
-  uint64_t w = __ldcg(reinterpret_cast<const unsigned long long*>(p));
-  if (check) {
-    Poll pl;
-    while (word_stamp(w) != stamp && pl.again(pp)) w = __ldcg(reinterpret_cast<const unsigned long long*>(p));
-  }
-  return word_value(w);
-}
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -414,7 +403,7 @@ __device__ __forceinline__ float residual_at(const Epi& e, int r) {
 }
 __device__ __forceinline__ void epi_write(const Epi& e, int r, float v) {
   if (e.flags & EF_WITHHOLD) return;
-  if (e.flags & EF_OUT_STAMPED) static_cast<uint64_t*>(e.out)[r] = stamp_word(v, e.stamp);
+  if (e.flags & EF_OUT_STAMPED) st_relaxed_u64(static_cast<uint64_t*>(e.out) + r, stamp_word(v, e.stamp));
   else static_cast<float*>(e.out)[r] = v;
 }
 
@@ -440,7 +429,8 @@ __device__ __forceinline__ float4 gain_block(const ActSrc& src, int j) {
 // shared memory by all consumer threads together (16-byte loads through L2, thread t taking blocks
 // t, t + NCT, ...): every warp of every CTA reading the same few cache lines serialises on those
 // lines, one read per CTA does not, and the load path does not queue behind the CTA's own bulk
-// weight copies. Stamped sources are read again, block by block, until the writers' stamps show.
+// weight copies. Stamped sources are read again, all stale blocks of a thread together, until the
+// writers' stamps show.
 // With an RMSNorm gain the stored values are x * g and the sum of squares of x is reduced on the
 // way; the return value is 1 / rms(x) (1 without a norm), the same in every consumer thread.
 // Returns after the named barrier that publishes the copy; the CTA's abort flag is then set (the
@@ -456,29 +446,47 @@ __device__ __forceinline__ float fetch_vector_n(Pipe& pp, const ActSrc& src, int
     if (src.xw) {
       // two 16-byte loads per block of 4 stamped words; stale blocks are read again until their
       // writers' stamps show (bounded)
-      const ulonglong2* xw = reinterpret_cast<const ulonglong2*>(src.xw);
+      const uint64_t* xw = src.xw;
       ulonglong2 w0[IF], w1[IF];
 #pragma unroll
       for (int u = 0; u < IF; ++u) {
         const int j = j0 + u * NCT;
         if (j < nb) {
-          w0[u] = __ldcg(xw + 2 * j);
-          w1[u] = __ldcg(xw + 2 * j + 1);
+          w0[u] = ld_relaxed_v2u64(xw + 4 * j);
+          w1[u] = ld_relaxed_v2u64(xw + 4 * j + 2);
+        }
+      }
+      if (src.check) {
+        // every block still stale is read again in the same turn, so that one more L2 round trip
+        // settles all of them (reading them again one after another would take one per block)
+        const unsigned sv = src.stamp;
+        auto fresh = [&](int u) {
+          return word_stamp(w0[u].x) == sv && word_stamp(w0[u].y) == sv && word_stamp(w1[u].x) == sv &&
+                 word_stamp(w1[u].y) == sv;
+        };
+        unsigned stale = 0;
+#pragma unroll
+        for (int u = 0; u < IF; ++u)
+          if (j0 + u * NCT < nb && !fresh(u)) stale |= 1u << u;
+        Poll pl;
+        while (stale && pl.again(pp)) {
+#pragma unroll
+          for (int u = 0; u < IF; ++u) {
+            if (stale & (1u << u)) {
+              const int j = j0 + u * NCT;
+              w0[u] = ld_relaxed_v2u64(xw + 4 * j);
+              w1[u] = ld_relaxed_v2u64(xw + 4 * j + 2);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < IF; ++u)
+            if ((stale & (1u << u)) && fresh(u)) stale &= ~(1u << u);
         }
       }
 #pragma unroll
       for (int u = 0; u < IF; ++u) {
         const int j = j0 + u * NCT;
         if (j < nb) {
-          if (src.check) {
-            const unsigned sv = src.stamp;
-            Poll pl;
-            while ((word_stamp(w0[u].x) != sv || word_stamp(w0[u].y) != sv || word_stamp(w1[u].x) != sv ||
-                    word_stamp(w1[u].y) != sv) && pl.again(pp)) {
-              w0[u] = __ldcg(xw + 2 * j);
-              w1[u] = __ldcg(xw + 2 * j + 1);
-            }
-          }
           x[u] = make_float4(word_value(w0[u].x), word_value(w0[u].y), word_value(w1[u].x), word_value(w1[u].y));
         } else {
           x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -526,10 +534,7 @@ __device__ __forceinline__ float fetch_vector_n(Pipe& pp, const ActSrc& src, int
   return 1.f / sqrtf(tot / (float)src.n + src.eps);
 }
 
-// Four blocks in flight per thread and turn (more would spill the persistent kernel's registers).
-__device__ __forceinline__ float fetch_vector(Pipe& pp, const ActSrc& src, int tid) {
-  return fetch_vector_n<4>(pp, src, tid);
-}
+
 
 // One lane's chunk of the input vector from the shared-memory copy: E / 4 consecutive 16-byte blocks
 // starting at block `blk0`. Lanes of a warp own chunks 32 or 128 bytes apart, so the blocks are
@@ -565,6 +570,15 @@ __device__ __forceinline__ void load_chunk(const float4* xs, int blk0, int lane,
   }
 }
 
+// Everything a GEMV phase needs that does not depend on other CTAs' results of the previous phase:
+// the matrix, this CTA's rows, where the input vector comes from and the epilogue.
+struct GemvPlan {
+  GemvDesc g;
+  RowSplit rs;
+  ActSrc src;
+  Epi epi;
+};
+
 // Consumes one CTA's rows [rs.r0, rs.r1) of a matrix from the ring ("How I built an LLM inference
 // engine from scratch in CUDA", v0.1 and "Round 1": a warp per row, 16-byte lane loads, several
 // rows per warp; here the rows come from the shared-memory ring instead of global memory).
@@ -574,26 +588,9 @@ __device__ __forceinline__ void load_chunk(const float4* xs, int blk0, int lane,
 // butterfly reduction. The LM head applies its epilogue in the warp; every other matrix leaves its
 // per-segment row results in shared memory, and one pass at the end of the phase sums the
 // segments in a fixed order and applies the epilogue (bias, residual add, SwiGLU on gate/up pairs).
-// Everything a GEMV phase needs that does not depend on other CTAs' results of the previous phase.
-// The persistent kernel builds it between its arrival at the grid barrier and its wait, so that
-// its cost (descriptors, the row split, cold code, the residual or bias operand) hides under the
-// barrier wait instead of adding to the phase.
-struct GemvPlan {
-  GemvDesc g;
-  RowSplit rs;
-  ActSrc src;
-  Epi epi;
-};
-
-// Completes a plan whose g, rs, src and epi are set: loads the early epilogue operand (the residual
-// rows are this CTA's own from its previous write, or the constant bias) and the thread's RMSNorm
-// gain blocks (constants: their first touch may miss to HBM, which the barrier wait then hides).
-__device__ __forceinline__ void gemv_plan_finish(Pipe& pp, GemvPlan& pl, int tid) {
-  (void)pp;
-  (void)tid;
-}
-
-template <int FMT, int NCHL>
+// IF: input blocks in flight per thread while fetching the input vector (four: eight made the
+// Llama-shaped bf16 step 8 % slower and the int4 instances spill).
+template <int FMT, int NCHL, int IF = 4>
 __device__ __forceinline__ bool gemv_rows(Pipe& pp, const GemvPlan& pl, Best& best, int tid,
                           unsigned long long* tr_ready) {
   constexpr int E = FMT == 0 ? 8 : 32;
@@ -621,7 +618,7 @@ __device__ __forceinline__ bool gemv_rows(Pipe& pp, const GemvPlan& pl, Best& be
   // Chunks past the segment read the segment's last chunk slot and are zeroed, so that the row loop
   // needs no per-lane branches
   if (tr_ready && tid == 0) tr_ready[TR_ENTRY - TR_READY] = globaltimer();
-  const float inv = fetch_vector(pp, src, tid);
+  const float inv = fetch_vector_n<IF>(pp, src, tid);
   if (tr_ready && tid == 0) tr_ready[TR_FETCHED - TR_READY] = globaltimer();
   if (*reinterpret_cast<volatile int*>(&pp.ms->abort)) return false;  // uniform after the fetch
   (void)norm;
@@ -886,7 +883,8 @@ struct AttnArgs {
   uint64_t* pow_ = nullptr;
   uint16_t* kc;            // this layer's K cache [nkv][max_ctx][d]
   uint16_t* vc;
-  const float2* rope;      // [max_ctx][d/2]
+  const float2* rope;      // RoPE table rows [rope_pos0, ...][d/2]
+  int rope_pos0 = 0;       // position of the table's first row (0: the full table)
   float* part_m;
   float* part_l;
   float* part_o;
@@ -991,7 +989,7 @@ static __device__ void attn_merge(const AttnArgs& A, Misc* ms, int tid, int j, i
     }
     const float r = num / ms->hl[g];
     const size_t oi = (size_t)h * d + i;
-    if (A.outw) A.outw[oi] = stamp_word(r, A.stamp_out);
+    if (A.outw) st_relaxed_u64(A.outw + oi, stamp_word(r, A.stamp_out));
     else A.out[oi] = r;
   }
 }
@@ -1124,23 +1122,15 @@ static __device__ bool attn_unit(Pipe& pp, const AttnArgs& A, const AttnSplit& s
   const int nk = max(0, min(t1, pos) - t0);  // cached positions, streamed through the ring
   const int T = max(0, t1 - t0);             // positions of the chunk: nk, plus pos itself
   const float scale = 1.f / sqrtf((float)d);
-  const float2* rt = A.rope + (size_t)pos * half;
+  const float2* rt = A.rope + (size_t)(pos - A.rope_pos0) * half;
   const size_t qo = (size_t)j * G * d;                      // q of the group's heads
   const size_t ko = (size_t)A.nq * d + (size_t)j * d;       // k of KV head j
   const size_t vo = ko + (size_t)A.nkv * d;                 // v of KV head j
-  // inputs: every load is issued first (stamped words, or plain floats as their bits), then each is
-  // settled -- for stamped words by waiting for the stamp of the QKV phase
+  // inputs: every load is issued first (stamped words, or plain floats as their bits); for stamped
+  // words every stale one is then read again in the same turn until the QKV phase's stamps show
   auto raw = [&](size_t i) -> uint64_t {
-    return A.qkvw ? (uint64_t)__ldcg(reinterpret_cast<const unsigned long long*>(A.qkvw + i))
+    return A.qkvw ? ld_relaxed_u64(A.qkvw + i)
                   : (uint64_t)__float_as_uint(__ldcg(A.qkv + i));
-  };
-  auto settle = [&](uint64_t w, size_t i) -> float {
-    if (A.qkvw && A.check) {
-      Poll pl;
-      while (word_stamp(w) != A.stamp_in && pl.again(pp))
-        w = __ldcg(reinterpret_cast<const unsigned long long*>(A.qkvw + i));
-    }
-    return word_value(w);
   };
   float* qs = sptr_w<float>(smem_addr(ms->at.qs));
   float* sc = sptr_w<float>(smem_addr(ms->at.sc));
@@ -1148,29 +1138,47 @@ static __device__ bool attn_unit(Pipe& pp, const AttnArgs& A, const AttnSplit& s
   float* vn = sptr_w<float>(smem_addr(ms->at.vn));
 
   constexpr int QR = (G_MAX * D_MAX / 2 + NCT - 1) / NCT;  // query pairs per thread, at most
-  uint64_t wq[QR][2];
-  size_t iq[QR][2];
+  constexpr int NW = 2 * QR + 3;                            // words per thread: q pairs, k pair, v
+  uint64_t wd[NW];
+  size_t ix[NW];
+  unsigned need = 0;  // the words this thread reads
 #pragma unroll
   for (int r = 0; r < QR; ++r) {
     const int idx = tid + r * NCT;
     if (idx < G * half) {
       const int g = idx / half, i = idx - g * half;
-      iq[r][0] = qo + g * d + i;
-      iq[r][1] = qo + g * d + i + half;
-      wq[r][0] = raw(iq[r][0]);
-      wq[r][1] = raw(iq[r][1]);
+      ix[2 * r] = qo + g * d + i;
+      ix[2 * r + 1] = qo + g * d + i + half;
+      need |= 3u << (2 * r);
     }
   }
   const bool hk = has_pos && tid < half, hv = has_pos && tid < d;
-  uint64_t wk0 = 0, wk1 = 0, wv = 0;
-  if (hk) { wk0 = raw(ko + tid); wk1 = raw(ko + tid + half); }
-  if (hv) wv = raw(vo + tid);
+  if (hk) { ix[2 * QR] = ko + tid; ix[2 * QR + 1] = ko + tid + half; need |= 3u << (2 * QR); }
+  if (hv) { ix[2 * QR + 2] = vo + tid; need |= 1u << (2 * QR + 2); }
+#pragma unroll
+  for (int e = 0; e < NW; ++e) wd[e] = (need & (1u << e)) ? raw(ix[e]) : 0;
+  if (A.qkvw && A.check) {
+    const unsigned sv = A.stamp_in;
+    unsigned stale = 0;
+#pragma unroll
+    for (int e = 0; e < NW; ++e)
+      if ((need & (1u << e)) && word_stamp(wd[e]) != sv) stale |= 1u << e;
+    Poll pl;
+    while (stale && pl.again(pp)) {
+#pragma unroll
+      for (int e = 0; e < NW; ++e)
+        if (stale & (1u << e)) wd[e] = ld_relaxed_u64(A.qkvw + ix[e]);
+#pragma unroll
+      for (int e = 0; e < NW; ++e)
+        if ((stale & (1u << e)) && word_stamp(wd[e]) == sv) stale &= ~(1u << e);
+    }
+  }
 #pragma unroll
   for (int r = 0; r < QR; ++r) {
     const int idx = tid + r * NCT;
     if (idx < G * half) {
       const int g = idx / half, i = idx - g * half;
-      const float x0 = settle(wq[r][0], iq[r][0]), x1 = settle(wq[r][1], iq[r][1]);
+      const float x0 = word_value(wd[2 * r]), x1 = word_value(wd[2 * r + 1]);
       const float2 cs = rt[i];
       qs[g * d + i] = (x0 * cs.x - x1 * cs.y) * scale;
       qs[g * d + i + half] = (x1 * cs.x + x0 * cs.y) * scale;
@@ -1180,7 +1188,7 @@ static __device__ bool attn_unit(Pipe& pp, const AttnArgs& A, const AttnSplit& s
     const size_t slot = ((size_t)j * A.max_ctx + pos) * d;
     if (hk) {
       const int i = tid;
-      const float x0 = settle(wk0, ko + i), x1 = settle(wk1, ko + i + half);
+      const float x0 = word_value(wd[2 * QR]), x1 = word_value(wd[2 * QR + 1]);
       const float2 cs = rt[i];
       const uint16_t b0 = f_to_bf16_bits(x0 * cs.x - x1 * cs.y);
       const uint16_t b1 = f_to_bf16_bits(x1 * cs.x + x0 * cs.y);
@@ -1190,7 +1198,7 @@ static __device__ bool attn_unit(Pipe& pp, const AttnArgs& A, const AttnSplit& s
       kn[i + half] = bf16_to_f(b1);
     }
     if (hv) {
-      const uint16_t b = f_to_bf16_bits(settle(wv, vo + tid));
+      const uint16_t b = f_to_bf16_bits(word_value(wd[2 * QR + 2]));
       A.vc[slot + tid] = b;
       vn[tid] = bf16_to_f(b);
     }
@@ -1257,8 +1265,7 @@ static __device__ bool attn_unit(Pipe& pp, const AttnArgs& A, const AttnSplit& s
       const int h = j * G + g;
       const size_t oi = ((size_t)h * A.nch_cap + c) * d + 2 * i2;
       if (A.pow_) {
-        *reinterpret_cast<ulonglong2*>(A.pow_ + oi) =
-            make_ulonglong2(stamp_word(o.x, A.stamp_out), stamp_word(o.y, A.stamp_out));
+        st_relaxed_v2u64(A.pow_ + oi, stamp_word(o.x, A.stamp_out), stamp_word(o.y, A.stamp_out));
       } else {
         *reinterpret_cast<float2*>(A.part_o + oi) = o;
       }
@@ -1269,8 +1276,8 @@ static __device__ bool attn_unit(Pipe& pp, const AttnArgs& A, const AttnSplit& s
     const int h = j * G + tid;
     const size_t mi = (size_t)h * A.nch_cap + c;
     if (A.pmw) {
-      A.pmw[mi] = stamp_word(ms->hm[tid], A.stamp_out);
-      A.plw[mi] = stamp_word(ms->hl[tid], A.stamp_out);
+      st_relaxed_u64(A.pmw + mi, stamp_word(ms->hm[tid], A.stamp_out));
+      st_relaxed_u64(A.plw + mi, stamp_word(ms->hl[tid], A.stamp_out));
     } else {
       A.part_m[mi] = ms->hm[tid];
       A.part_l[mi] = ms->hl[tid];
@@ -1308,21 +1315,8 @@ static __device__ bool attn_merge_slice(Pipe& pp, const AttnArgs& A, const AttnS
   const int o0 = c * per, o1 = min(o0 + per, nout);
   const unsigned sv = A.stamp_out;
   const bool check = A.check != 0;
-  auto get = [&](const uint64_t* p) -> float {
-    uint64_t w = __ldcg(reinterpret_cast<const unsigned long long*>(p));
-    if (check) {
-      Poll pl;
-      while (word_stamp(w) != sv && pl.again(pp)) w = __ldcg(reinterpret_cast<const unsigned long long*>(p));
-    }
-    return word_value(w);
-  };
-  auto word = [&](const uint64_t* p) -> uint64_t {
-    return __ldcg(reinterpret_cast<const unsigned long long*>(p));
-  };
-  auto val = [&](uint64_t w, const uint64_t* p) -> float {
-    return word_stamp(w) == sv || !check ? word_value(w) : get(p);
-  };
-  // two outputs per warp and pass: all six loads of a chunk batch are issued before any is used
+  // two outputs per warp and pass: all six loads of a chunk batch are issued before any is used,
+  // and every stale one is read again in the same turn until its sibling's stamp shows
   for (int oa = o0 + warp; oa < o1; oa += 2 * NCW) {
     const int ob = oa + NCW;
     const bool hb = ob < o1;  // warp-uniform
@@ -1333,23 +1327,39 @@ static __device__ bool attn_merge_slice(Pipe& pp, const AttnArgs& A, const AttnS
       const int cc = cb + lane;
       const bool on = cc < nch;
       const size_t mia = (size_t)ha * A.nch_cap + cc, mib = (size_t)hb_ * A.nch_cap + cc;
-      uint64_t wma = 0, wla = 0, woa = 0, wmb = 0, wlb = 0, wob = 0;
-      if (on) {
-        wma = word(A.pmw + mia); wla = word(A.plw + mia); woa = word(A.pow_ + mia * d + ia);
-        if (hb) { wmb = word(A.pmw + mib); wlb = word(A.plw + mib); wob = word(A.pow_ + mib * d + ib); }
+      const uint64_t* src[6] = {A.pmw + mia, A.plw + mia, A.pow_ + mia * d + ia,
+                                A.pmw + mib, A.plw + mib, A.pow_ + mib * d + ib};
+      const unsigned need = on ? (hb ? 0x3Fu : 0x07u) : 0u;
+      uint64_t w[6];
+#pragma unroll
+      for (int e = 0; e < 6; ++e) w[e] = (need & (1u << e)) ? ld_relaxed_u64(src[e]) : 0;
+      if (check) {
+        unsigned stale = 0;
+#pragma unroll
+        for (int e = 0; e < 6; ++e)
+          if ((need & (1u << e)) && word_stamp(w[e]) != sv) stale |= 1u << e;
+        Poll pl;
+        while (stale && pl.again(pp)) {
+#pragma unroll
+          for (int e = 0; e < 6; ++e)
+            if (stale & (1u << e)) w[e] = ld_relaxed_u64(src[e]);
+#pragma unroll
+          for (int e = 0; e < 6; ++e)
+            if ((stale & (1u << e)) && word_stamp(w[e]) == sv) stale &= ~(1u << e);
+        }
       }
       float ma = -CUDART_INF_F, la = 0.f, va = 0.f, mb = -CUDART_INF_F, lb = 0.f, vb = 0.f;
       if (on) {
-        ma = val(wma, A.pmw + mia); la = val(wla, A.plw + mia); va = val(woa, A.pow_ + mia * d + ia);
-        if (hb) { mb = val(wmb, A.pmw + mib); lb = val(wlb, A.plw + mib); vb = val(wob, A.pow_ + mib * d + ib); }
+        ma = word_value(w[0]); la = word_value(w[1]); va = word_value(w[2]);
+        if (hb) { mb = word_value(w[3]); lb = word_value(w[4]); vb = word_value(w[5]); }
       }
       if (tr && tid == 0 && cb == 0 && oa == o0) tr[TR_AUX1] = globaltimer();  // siblings' partials seen
       merge_step(Ma, na, da, ma, la, va);
       if (hb) merge_step(Mb, nb, db, mb, lb, vb);
     }
     if (lane == 0) {
-      A.outw[(size_t)ha * d + ia] = stamp_word(na / da, A.stamp_out);
-      if (hb) A.outw[(size_t)hb_ * d + ib] = stamp_word(nb / db, A.stamp_out);
+      st_relaxed_u64(A.outw + (size_t)ha * d + ia, stamp_word(na / da, A.stamp_out));
+      if (hb) st_relaxed_u64(A.outw + (size_t)hb_ * d + ib, stamp_word(nb / db, A.stamp_out));
     }
   }
   named_sync(BAR_CONS, NCT);

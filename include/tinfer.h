@@ -43,7 +43,8 @@ typedef enum {
   TINFER_ERR_CUDA = 3,          /* a CUDA runtime call failed (launch, capture, copy) */
   TINFER_ERR_OOM = 4,           /* a device or pinned-host allocation failed */
   TINFER_ERR_NONFINITE = 5,     /* a logit was NaN or infinite (the argmax output is -1) */
-  TINFER_ERR_TIMEOUT = 6        /* a device-side wait gave up (grid barrier, pipeline stage) */
+  TINFER_ERR_TIMEOUT = 6        /* a device-side wait gave up (a phase's stamped results or a
+                                   pipeline stage that never arrived) */
 } tinfer_status;
 
 enum { TINFER_BF16 = 0, TINFER_INT4 = 1 };              /* weight_format */
@@ -106,15 +107,24 @@ tinfer_status tinfer_unpack_layer(const tinfer_config* cfg, const void* packed_d
                                   const tinfer_layer_src* dst, void* stream);
 
 /* Creates an engine over borrowed weights and a borrowed KV cache (k_cache_dev, v_cache_dev: bf16
- * [n_layers][n_kv_heads][max_ctx][head_dim]). The context owns its scratch (activations, split-K
- * partials, barrier and ticket words, argmax slots, the fp32 RoPE cos/sin table, the CUDA graph in
- * graph mode) and frees it in tinfer_destroy. Uses the current CUDA device. */
+ * [n_layers][n_kv_heads][max_ctx][head_dim]). Set-up happens once per model and GPU, and every
+ * launch after it follows the same fixed schedule ("Decoding in tiles", section 4: the plan is made
+ * and validated once, and the launch makes no scheduling decision). The context owns its scratch
+ * (stamped hand-off buffers, split-K partials, ticket words, argmax slots, the fp32 RoPE cos/sin
+ * table, the CUDA graph in graph mode) and frees it in tinfer_destroy. Uses the current CUDA device.
+ * Weights, scales and the KV cache must be 16-byte aligned; a NULL or misaligned pointer returns
+ * TINFER_ERR_INVALID_ARG, an unsupported shape TINFER_ERR_UNSUPPORTED, a failed allocation
+ * TINFER_ERR_OOM, all before anything is launched. */
 tinfer_status tinfer_create(const tinfer_config* cfg, const tinfer_weights* w, void* k_cache_dev,
                             void* v_cache_dev, tinfer_ctx** out);
 
-/* One decode step for token_id at position pos on `stream`. logits_dev (fp32 [vocab]) may be NULL
- * to skip writing the logits; argmax_dev (int32 [1]) receives the greedy token, the lowest id among
- * equal maxima, or -1 when a logit is non-finite. Returns at once (asynchronous). */
+/* One decode step for token_id at position pos on `stream` ("Decoding in tiles", section 5 "One
+ * token, end to end": every layer, the final norm, lm_head and a greedy choice on the device, the
+ * largest logit with the lowest token id among ties, an error word on a non-finite logit).
+ * logits_dev (fp32 [vocab]) may be NULL to skip writing the logits; argmax_dev (int32 [1]) receives
+ * the greedy token, or -1 when a logit is non-finite. Returns at once (asynchronous).
+ * token_id outside [0, vocab) or pos outside [0, max_ctx) returns TINFER_ERR_INVALID_ARG without
+ * launching; so does an error a previous step left in the error word (its own status). */
 tinfer_status tinfer_decode_step(tinfer_ctx* ctx, int32_t token_id, int32_t pos, void* stream,
                                  float* logits_dev, int32_t* argmax_dev);
 
@@ -131,8 +141,11 @@ tinfer_status tinfer_decode_step_dev(tinfer_ctx* ctx, const int32_t* token_dev, 
 tinfer_status tinfer_generate(tinfer_ctx* ctx, int32_t first_token, int32_t pos0, int32_t n_steps,
                               void* stream, int32_t* tokens_host);
 
-/* Waits for all work of the context, then returns and clears the device error word
- * (TINFER_OK if none). Clearing also resets the context's barrier and ticket words. */
+/* Waits for all work of the context, then returns and clears the device error word (TINFER_OK if
+ * none): TINFER_ERR_NONFINITE for a non-finite logit, TINFER_ERR_TIMEOUT for a device wait that ran
+ * out, TINFER_ERR_INVALID_ARG for an out-of-range device token ("Decoding in tiles", section 5:
+ * worker 0 records the token, the count, the end flag and an error code for the host). Clearing
+ * also resets the context's ticket words. Synchronises the device. */
 tinfer_status tinfer_get_error(tinfer_ctx* ctx);
 
 /* Introspection: TINFER_Q_GRID (CTAs of the persistent launch = SM count), TINFER_Q_SMEM (dynamic
@@ -148,21 +161,37 @@ long long tinfer_query(const tinfer_ctx* ctx, int what);
  * memory of TINFER_Q_TRACE_BYTES bytes, caller-owned), every following megakernel step writes, for
  * every CTA c and phase k (k = 5*layer + {0 QKV, 1 attention, 2 O, 3 gate/up, 4 down}, the LM head
  * last), ten uint64 %globaltimer nanosecond stamps at [(c * phases + k) * 10 + f] (0 where nothing
- * was recorded): f = 0 phase start (after the previous grid barrier), 2 phase end, 3 producer starts
+ * was recorded): f = 0 phase start (the CTA is done with the previous phase), 2 phase end, 3 producer starts
  * issuing the phase's copies, 4 producer has issued them; GEMV phases: 1 activations normalised and
  * ready, 5 input activations in registers, 6 GEMV code entered, 7 input vector in shared memory,
  * 8 first weight stage available, 9 last weight stage consumed;
  * attention phases (first unit of the CTA): 1 keys arrived, 5 queries rotated, 6 scores done,
- * 7 partials written, 8 values arrived, 9 merge started (CTAs that merge). NULL turns tracing off. */
+ * 7 partials written, 8 values arrived, 9 the merge has seen every sibling's partials (first unit
+ * of the CTA). NULL turns tracing off. */
 tinfer_status tinfer_set_trace(tinfer_ctx* ctx, void* trace_dev);
 
 /* Test hooks: timeout of every device-side wait in nanoseconds (default 200 ms), and a fault
  * injected on the host side of the contract: in the next persistent step, CTA `cta` withholds its
- * results of GEMV phase number `barrier` (k = 5*layer + {0 QKV, 2 O, 3 gate/up, 4 down}; the LM head
+ * results of GEMV phase number `phase` (k = 5*layer + {0 QKV, 2 O, 3 gate/up, 4 down}; the LM head
  * 5*n_layers), so that the CTAs waiting for them run out of time and the step reports
- * TINFER_ERR_TIMEOUT (cta = -1 disables; a CTA without rows in that phase withholds nothing). */
+ * TINFER_ERR_TIMEOUT (cta = -1 disables; a CTA without rows in that phase withholds nothing).
+ * TINFER_ERR_UNSUPPORTED in graph mode. */
 tinfer_status tinfer_set_timeout_ns(tinfer_ctx* ctx, long long ns);
-tinfer_status tinfer_debug_skip_barrier(tinfer_ctx* ctx, int cta, int barrier);
+tinfer_status tinfer_debug_withhold_results(tinfer_ctx* ctx, int cta, int phase);
+
+/* The producer's schedule ("Decoding in tiles", section 1: Hazy Research's kernel overlaps the next
+ * instruction's loads with the current one; section 4: TileInfer does not): how far the weight
+ * stream runs ahead of the consumers. TINFER_S_INFLIGHT: bulk copies outstanding per CTA (default
+ * 2; clamped to the ring's stages, 0 = the whole ring); TINFER_S_INFLIGHT_LM: the same during the LM
+ * head (default 4); TINFER_S_L2_LOOKAHEAD: bytes per CTA prefetched into L2 ahead of the ring while
+ * the ring is full (default 512 KiB for bf16 models, 0 for int4); TINFER_S_L2_PACE: nanoseconds per
+ * KiB between those prefetches (default 24, about one SM's share of HBM bandwidth). Values outside
+ * [0, 64 MiB] (lookahead), [0, 100000] (pace) or [0, 8] (copies) return TINFER_ERR_INVALID_ARG.
+ * Takes effect from the next step; results do not depend on it. tinfer_get_schedule returns the
+ * current value, or -1 for an unknown knob. */
+enum { TINFER_S_INFLIGHT = 0, TINFER_S_INFLIGHT_LM = 1, TINFER_S_L2_LOOKAHEAD = 2, TINFER_S_L2_PACE = 3 };
+tinfer_status tinfer_set_schedule(tinfer_ctx* ctx, int knob, long long value);
+long long tinfer_get_schedule(const tinfer_ctx* ctx, int knob);
 
 void tinfer_destroy(tinfer_ctx* ctx);
 

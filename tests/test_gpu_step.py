@@ -175,7 +175,7 @@ def test_barrier_timeout_is_reported_and_the_context_recovers():
     w = synth.make_model(c)
     eng = T.Engine(c, w)
     assert T.tinfer_set_timeout_ns(eng.ctx, 20_000_000) == 0
-    assert T.tinfer_debug_skip_barrier(eng.ctx, 3, 2) == 0
+    assert T.tinfer_debug_withhold_results(eng.ctx, 3, 2) == 0
     eng.step(5, 0)
     assert eng.error() == T.TINFER_ERR_TIMEOUT
     # the same step again, now without the fault, matches a fresh engine

@@ -52,3 +52,20 @@ def kv_close(gpu_bits, ref_bits, rel_floor=2e-4):
     floor = rel_floor * float(np.sqrt(np.mean(b * b)))
     tol = np.maximum(np.abs(a), np.abs(b)) * 2.0 ** -7 + floor
     return float((np.abs(a - b) - tol).max())
+
+
+def kv_deviation(gpu_bits, ref_bits):
+    """How GPU-written KV values (fp32 arithmetic, rounded to bf16) differ from the oracle's (fp64,
+    rounded to bf16): the largest deviation in bf16 steps among values of magnitude at least 1/16 of
+    the reference RMS, and the largest absolute deviation of the smaller values in multiples of that
+    RMS (near zero a bf16 step is tiny, and the fp32 error carried by the residual stream and the
+    dot product is what remains)."""
+    a = bf16_to_f64(gpu_bits)
+    b = bf16_to_f64(ref_bits)
+    d = np.abs(a - b)
+    rms = float(np.sqrt(np.mean(b * b)))
+    big = np.abs(b) >= rms / 16
+    step = np.maximum(np.abs(a), np.abs(b)) * 2.0 ** -7
+    steps_big = float((d[big] / step[big]).max()) if big.any() else 0.0
+    small_rms = float(d[~big].max() / rms) if (~big).any() and rms > 0 else 0.0
+    return steps_big, small_rms
