@@ -270,6 +270,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-loop", action="store_true", help="skip the in-kernel token loop measurement")
     ap.add_argument("--no-read-probe", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=0, help="steps of the e2e run (default: the workload's)")
     args = ap.parse_args()
@@ -334,6 +335,33 @@ def main():
                              grid=eng.query(T.TINFER_Q_GRID), smem=eng.query(T.TINFER_Q_SMEM),
                              threads=eng.query(T.TINFER_Q_BLOCK_THREADS),
                              stages=eng.query(T.TINFER_Q_RING_STAGES), slot=eng.query(T.TINFER_Q_SLOT_BYTES))
+        if name == "mega" and not args.no_loop:
+            # the in-kernel token loop: the workload's S steps in one launch (tinfer_generate_dev),
+            # timed on the device; then end to end through the same call with the first token from
+            # the host and every chosen token copied back to pinned host memory inside the region
+            toks_l = torch.zeros(S, dtype=torch.int32, device="cuda")
+            host_l = torch.zeros(S, dtype=torch.int32).pin_memory()
+            assert T.tinfer_generate_dev(eng.ctx, first, P, S, -1, st, toks_l, None) == 0
+            torch.cuda.synchronize()
+            reps = max(1, int(np.ceil(MIN_TIMED_S * 1e3 / (S * results[name]["ms_step"]))))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            barrier(dist, torch)
+            e0.record(st)
+            for _ in range(reps):
+                assert T.tinfer_generate_dev(eng.ctx, first, P, S, -1, st, toks_l, None) == 0
+            e1.record(st)
+            barrier(dist, torch)
+            ms_l = max_over_ranks(dist, torch, e0.elapsed_time(e1))
+            barrier(dist, torch)
+            t0 = time.perf_counter()
+            for _ in range(reps):
+                assert T.tinfer_generate_dev(eng.ctx, first, P, S, -1, st, toks_l, None) == 0
+                host_l.copy_(toks_l, non_blocking=True)
+                st.synchronize()
+            el_l = max_over_ranks(dist, torch, time.perf_counter() - t0)
+            assert eng.error() == T.TINFER_OK
+            results["loop"] = dict(ms_token=ms_l / (reps * S), tokens=reps * S, launches=reps,
+                                   e2e=world * reps * S / el_l)
         if name == modes[0][0]:
             # end to end through the public call: host-in-the-loop greedy generation, one pinned
             # 4-byte token copied in and one 4-byte choice copied out per step
@@ -420,6 +448,14 @@ def main():
         "launch": {"grid": r["grid"], "threads": r["threads"], "smem": r["smem"], "ring_stages": r["stages"],
                    "slot_bytes": r["slot"]},
     }
+    if "loop" in results:
+        lp = results["loop"]
+        line["token_loop"] = {"tokens/s": world * 1e3 / lp["ms_token"], "ms_per_token": lp["ms_token"],
+                              "tokens_per_launch": S, "launches": lp["launches"],
+                              "achieved_gbs": bytes_step / (lp["ms_token"] * 1e-3) / 1e9,
+                              "e2e": {"value": lp["e2e"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                                      "d2h_bytes_per_step": 4},
+                              "call": "tinfer_generate_dev (one cooperative launch per window)"}
     if "graph" in results and main_mode == "mega":
         g = results["graph"]
         line["graph_baseline"] = {"tokens/s": world * g["steps"] / (g["ms_total"] * 1e-3),

@@ -27,7 +27,7 @@ TRACE_FIELDS = 10  # stamps per CTA and phase of the timeline (tinfer_set_trace)
 EXPORTS = [
     "tinfer_status_string", "tinfer_check_config", "tinfer_packed_layer_bytes", "tinfer_pack_layer",
     "tinfer_unpack_layer", "tinfer_create", "tinfer_decode_step", "tinfer_decode_step_dev",
-    "tinfer_generate", "tinfer_get_error", "tinfer_query", "tinfer_set_trace", "tinfer_set_timeout_ns",
+    "tinfer_generate", "tinfer_generate_dev", "tinfer_get_error", "tinfer_query", "tinfer_set_trace", "tinfer_set_timeout_ns",
     "tinfer_debug_withhold_results", "tinfer_set_schedule", "tinfer_get_schedule", "tinfer_destroy",
     "tinfer_packed_row_bytes", "tinfer_pack_matrix", "tinfer_op_gemv", "tinfer_op_attention",
     "tinfer_op_attention_noalloc",
@@ -86,6 +86,7 @@ def lib():
             "tinfer_decode_step": ([P, ctypes.c_int32, ctypes.c_int32, P, P, P], I),
             "tinfer_decode_step_dev": ([P, P, ctypes.c_int32, P, P, P], I),
             "tinfer_generate": ([P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P, P], I),
+            "tinfer_generate_dev": ([P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P, P, P], I),
             "tinfer_get_error": ([P], I),
             "tinfer_query": ([P, I], LL),
             "tinfer_set_trace": ([P, P], I),
@@ -175,6 +176,12 @@ def tinfer_generate(ctx, first_token: int, pos0: int, n_steps: int, stream, toke
     else:
         ptr = ctypes.addressof(tokens_host)
     return lib().tinfer_generate(ctx, int(first_token), int(pos0), int(n_steps), _stream(stream), ptr)
+
+
+def tinfer_generate_dev(ctx, first_token: int, pos0: int, n_steps: int, eos_token: int, stream, tokens_dev,
+                        count_dev=None) -> int:
+    return lib().tinfer_generate_dev(ctx, int(first_token), int(pos0), int(n_steps), int(eos_token),
+                                     _stream(stream), _ptr(tokens_dev), _ptr(count_dev))
 
 
 def tinfer_get_error(ctx) -> int:

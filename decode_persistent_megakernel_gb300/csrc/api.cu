@@ -375,6 +375,7 @@ tinfer_status tinfer_create(const tinfer_config* c, const tinfer_weights* w, voi
   const size_t o_tk = take((size_t)(nkv + 1) * 4);
   const size_t o_bv = take((size_t)grid * 4), o_bi = take((size_t)grid * 4), o_bb = take((size_t)grid * 4);
   const size_t o_err = take(4), o_step = take(2 * 4), o_gen = take(2 * 4), o_am = take(4);
+  const size_t o_bw = take((size_t)grid * 16), o_kvf = take((size_t)c->n_layers * nkv * 4);
   if ((st = cu(cudaMalloc(&x->scratch, off))) != TINFER_OK) return fail(st);
   if ((st = cu(cudaMemset(x->scratch, 0, off))) != TINFER_OK) return fail(st);
   uint8_t* s = (uint8_t*)x->scratch;
@@ -447,6 +448,12 @@ tinfer_status tinfer_create(const tinfer_config* c, const tinfer_weights* w, voi
   x->gen_dev = (int*)(s + o_gen);
   x->argmax_fallback = (int*)(s + o_am);
   p.n_chunks_override = 0;
+  p.n_steps = 1;
+  p.tokens_out = nullptr;
+  p.count_out = nullptr;
+  p.eos = -1;
+  p.best_w = (uint64_t*)(s + o_bw);
+  p.kvflag = (unsigned*)(s + o_kvf);
   p.dbg_skip_cta = -1;
   p.dbg_skip_phase = -1;
   p.trace = nullptr;
@@ -540,6 +547,39 @@ tinfer_status tinfer_decode_step_dev(tinfer_ctx* x, const int32_t* token_dev, in
                                      void* stream, float* logits_dev, int32_t* argmax_dev) {
   if (!token_dev) return TINFER_ERR_INVALID_ARG;
   return step_impl(x, 0, token_dev, pos, (cudaStream_t)stream, logits_dev, argmax_dev);
+}
+
+tinfer_status tinfer_generate_dev(tinfer_ctx* x, int32_t first_token, int32_t pos0, int32_t n_steps,
+                                  int32_t eos_token, void* stream, int32_t* tokens_dev,
+                                  int32_t* count_dev) {
+  if (!x || n_steps <= 0 || !tokens_dev) return TINFER_ERR_INVALID_ARG;
+  if (pos0 < 0 || (long long)pos0 + n_steps > x->cfg.max_ctx) return TINFER_ERR_INVALID_ARG;
+  if (first_token < 0 || first_token >= x->cfg.vocab) return TINFER_ERR_INVALID_ARG;
+  if (eos_token < -1 || eos_token >= x->cfg.vocab) return TINFER_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(tokens_dev) & 3) || (reinterpret_cast<uintptr_t>(count_dev) & 3))
+    return TINFER_ERR_INVALID_ARG;
+  const int pending = *reinterpret_cast<volatile int*>(x->err_host);
+  if (pending) return status_of_word(pending);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (x->cfg.exec_mode != TINFER_MEGAKERNEL) {
+    // the baseline: one graph launch per token, chained on the device
+    if (eos_token >= 0 || count_dev) return TINFER_ERR_UNSUPPORTED;
+    for (int k = 0; k < n_steps; ++k)
+      TRY(step_impl(x, first_token, k ? tokens_dev + k - 1 : nullptr, pos0 + k, st, nullptr, tokens_dev + k));
+    return TINFER_OK;
+  }
+  StepParams p = x->p;
+  p.ring_stages = x->stages_mega;
+  p.token = first_token; p.token_dev = nullptr; p.pos = pos0;
+  p.logits = nullptr; p.argmax = x->argmax_fallback;
+  p.n_steps = n_steps;
+  p.tokens_out = tokens_dev;
+  p.count_out = count_dev;
+  p.eos = eos_token;
+  TRY_CUDA(launch_megakernel(p, x->smem_mega, st));
+  x->p.dbg_skip_cta = -1;
+  x->p.epoch += (unsigned)n_steps * (unsigned)(x->cfg.n_layers * PHASES_PER_LAYER + 2);
+  return TINFER_OK;
 }
 
 tinfer_status tinfer_get_error(tinfer_ctx* x) {

@@ -118,8 +118,16 @@ struct __align__(16) StepParams {
   int n_chunks_override;   // >0: fixed number of attention chunks (single-op test path)
   float* logits;           // [V] or null
   int* argmax;             // [1]
+  // the in-kernel token loop (persistent kernel): n_steps decode steps in one launch, step s at
+  // position pos + s, its token the greedy choice of step s - 1
+  int n_steps;             // 1: one step (argmax through the ticketed last CTA)
+  int* tokens_out;         // [n_steps] greedy token of every step (-1: a non-finite logit)
+  int* count_out;          // steps completed, or null
+  int eos;                 // stop after a step that chose this token (-1: never)
+  uint64_t* best_w;        // [grid][2] per-CTA best of the LM head as stamped words (value; index)
+  unsigned* kvflag;        // [nkv] token loop: the first stamp of the step whose K/V slot is visible
   int dbg_skip_cta;        // fault injection: CTA that withholds its results of one GEMV phase (-1 none)
-  int dbg_skip_phase;    // ... the phase index
+  int dbg_skip_phase;      // ... the phase index
   unsigned long long* trace;  // optional timeline [grid][phases][TRACE_FIELDS] of %globaltimer ns
 };
 

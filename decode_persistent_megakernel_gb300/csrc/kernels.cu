@@ -136,7 +136,7 @@ __global__ void f32_to_bf16_kernel(const float* in, uint16_t* out, int n) {
 // ------------------------------------------------------------------------------ launch wrappers
 
 // kernel instances of mega_bf16.cu / mega_int4.cu; kind 0: persistent kernel, 1: persistent kernel
-// recording a timeline, 2: per-phase kernel
+// recording a timeline, 2: per-phase kernel, 3: persistent kernel with the token loop
 const void* step_kernel_bf16(int nchl, int kind);
 const void* step_kernel_int4(int nchl, int kind);
 static const void* step_fn(int fmt, int nchl, int kind) {
@@ -144,7 +144,7 @@ static const void* step_fn(int fmt, int nchl, int kind) {
 }
 
 cudaError_t launch_megakernel(const StepParams& p, size_t smem, cudaStream_t st) {
-  const void* fn = step_fn(p.m.fmt, p.m.nchl, p.trace ? 1 : 0);
+  const void* fn = step_fn(p.m.fmt, p.m.nchl, p.n_steps > 1 ? 3 : p.trace ? 1 : 0);
   if (!fn) return cudaErrorInvalidDeviceFunction;
   void* args[] = {const_cast<StepParams*>(&p)};
   return cudaLaunchCooperativeKernel(fn, dim3(p.grid), dim3(NTHREADS_MEGA), args, smem, st);
@@ -211,8 +211,11 @@ static cudaError_t raise_limit(const void* fn, size_t bytes) {
   return cudaSuccess;
 }
 cudaError_t set_smem_mega(size_t b, int fmt, int nchl) {
-  cudaError_t e = raise_limit(step_fn(fmt, nchl, 0), b);
-  return e != cudaSuccess ? e : raise_limit(step_fn(fmt, nchl, 1), b);
+  for (int kind : {0, 1, 3}) {
+    const cudaError_t e = raise_limit(step_fn(fmt, nchl, kind), b);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 cudaError_t set_smem_phase(size_t b, int fmt, int nchl) { return raise_limit(step_fn(fmt, nchl, 2), b); }
 cudaError_t set_smem_op_gemv(size_t b) { return raise_limit((const void*)op_gemv_kernel, b); }

@@ -45,16 +45,26 @@ __device__ __forceinline__ GemvDesc phase_gemv(const StepParams& p, int phase, i
   return g;
 }
 
-// Attention of phase k (layer `layer`): q/k/v from the QKV phase k - 1, output for the O phase.
-__device__ __forceinline__ AttnArgs step_attn_args(const StepParams& p, int layer, int pos, int k) {
+// Stamps of the launch's step s: phase k of step s writes epoch + s * stride + k (stride: the
+// phases of a step plus one), so that stamps keep increasing across the steps of one launch.
+__device__ __forceinline__ int phases_per_step(const StepParams& p) { return p.m.L * PHASES_PER_LAYER + 1; }
+__device__ __forceinline__ unsigned step_epoch(const StepParams& p, int s) {
+  return p.epoch + (unsigned)s * (unsigned)(phases_per_step(p) + 1);
+}
+
+// Attention of phase k (layer `layer`) of the step whose stamps start at ep: q/k/v from the QKV phase
+// k - 1, output for the O phase.
+__device__ __forceinline__ AttnArgs step_attn_args(const StepParams& p, int layer, int pos, int k, unsigned ep,
+                                                   bool loop = false) {
+  (void)loop;
   const Dims& m = p.m;
   AttnArgs A;
   A.qkv = nullptr;
   A.qkvw = p.qkv;
-  A.stamp_in = p.epoch + (unsigned)(k - 1);
+  A.stamp_in = ep + (unsigned)(k - 1);
   A.check = p.stamp_check;
   A.outw = p.attn;
-  A.stamp_out = p.epoch + (unsigned)k;
+  A.stamp_out = ep + (unsigned)k;
   const size_t lay = (size_t)layer * m.nkv * m.max_ctx * m.d;
   A.kc = p.kcache + lay;
   A.vc = p.vcache + lay;
@@ -77,7 +87,7 @@ __device__ __forceinline__ AttnArgs step_attn_args(const StepParams& p, int laye
 __device__ __forceinline__ void produce_phase(const StepParams& p, Pipe& pp, int phase, int layer, int pos,
                               uint64_t pol_w, uint64_t pol_kv, bool& dead) {
   if (phase == PH_ATTN) {
-    const AttnArgs A = step_attn_args(p, layer, pos, 0);  // the producer uses the cache pointers only
+    const AttnArgs A = step_attn_args(p, layer, pos, 0, p.epoch);  // the producer uses the cache pointers only
     const AttnSplit sp = attn_split(pos, A.nkv, A.d, p.grid, p.slot_bytes, p.n_chunks_override);
     const int units = A.nkv * sp.nch;
     for (int u = blockIdx.x; u < units; u += p.grid)
@@ -98,9 +108,10 @@ __device__ __forceinline__ unsigned long long* trace_at(unsigned long long* trac
   return trace + ((size_t)blockIdx.x * nph + k) * TRACE_FIELDS + field;
 }
 
-// The persistent producer's view of the step: one pass over this CTA's copy schedule, stage by
+// The persistent producer's view of the launch: one pass over this CTA's copy schedule, stage by
 // stage, in the order the consumers take them (per GEMV phase its rows; per attention unit the
-// cached K chunk, then the V chunk).
+// cached K chunk, then the V chunk). k counts the phases of the whole launch; only the instance
+// with the token loop has more than one step, and only it tracks the step of a phase.
 struct StageCursor {
   int k, j;                        // phase index, stage within the phase
   int attn;                        // the phase is attention
@@ -109,18 +120,29 @@ struct StageCursor {
   const uint16_t* kc;              // attention: this layer's K and V caches
   const uint16_t* vc;
   int u, units, nch, cl, sub;      // unit cursor, split, K/V half of the unit
+  int klocal, pos;                 // token loop: phase index within its step, that step's position
+  int kvl;                         // token loop: that step's index
 };
 
-static __device__ void cursor_enter(const StepParams& p, StageCursor& c, int pos) {
-  const int nph = p.m.L * PHASES_PER_LAYER + 1;
-  if (c.k >= nph) return;
+template <bool LOOP>
+__device__ __forceinline__ void cursor_enter(const StepParams& p, StageCursor& c, int& pos, int n_steps) {
+  const int nph = phases_per_step(p);
+  if (c.k >= nph * n_steps) return;
+  int k = c.k, s = 0;
+  if constexpr (LOOP) {
+    s = c.k / nph;
+    k = c.k - s * nph;
+    c.klocal = k;
+    c.pos = pos = p.pos + s;
+  }
   int phase, layer;
-  phase_of(c.k, p.m.L, phase, layer);
+  phase_of(k, p.m.L, phase, layer);
   if (phase == PH_ATTN) {
     const AttnSplit sp = attn_split(pos, p.m.nkv, p.m.d, p.grid, p.slot_bytes, p.n_chunks_override);
     const size_t lay = (size_t)layer * p.m.nkv * p.m.max_ctx * p.m.d;
     c.attn = 1; c.kc = p.kcache + lay; c.vc = p.vcache + lay;
     c.nch = sp.nch; c.cl = sp.cl; c.units = p.m.nkv * sp.nch; c.u = blockIdx.x; c.sub = 0;
+    if constexpr (LOOP) c.kvl = s;
     return;
   }
   const GemvDesc g = phase_gemv(p, phase, layer);
@@ -129,10 +151,18 @@ static __device__ void cursor_enter(const StepParams& p, StageCursor& c, int pos
   c.j = 0;
 }
 
-static __device__ bool cursor_next(const StepParams& p, StageCursor& c, int pos, const void*& src,
-                            uint32_t& bytes) {
-  const int nph = p.m.L * PHASES_PER_LAYER + 1;
-  while (c.k < nph) {
+// The next stage's copy. In the token loop, *wait (when set) is the flag of a K/V slot another CTA
+// wrote in the previous step of this launch: the copy may be issued once the flag carries `stamp`.
+template <bool LOOP>
+__device__ __forceinline__ bool cursor_next(const StepParams& p, StageCursor& c, int pos, const void*& src,
+                                            uint32_t& bytes, const unsigned*& wait, unsigned& stamp,
+                                            int n_steps) {
+  const int nk_all = phases_per_step(p) * n_steps;
+  if constexpr (LOOP) {
+    wait = nullptr;
+    pos = c.pos;
+  }
+  while (c.k < nk_all) {
     if (!c.attn) {
       const int s0 = c.r0 + c.j * c.nr;
       if (s0 < c.r1) {
@@ -149,44 +179,56 @@ static __device__ bool cursor_next(const StepParams& p, StageCursor& c, int pos,
       const size_t base = ((size_t)j * p.m.max_ctx + t0) * p.m.d;
       src = (c.sub == 0 ? c.kc : c.vc) + base;
       bytes = (uint32_t)(nk * p.m.d * 2);
+      if constexpr (LOOP) {
+        if (c.kvl > 0 && nk > 0 && tend == pos) {  // holds slot pos - 1, written by the previous step
+          wait = p.kvflag + j;
+          stamp = step_epoch(p, c.kvl - 1);
+        }
+      }
       if (c.sub) { c.sub = 0; c.u += p.grid; } else { c.sub = 1; }
       return true;
     }
     ++c.k;
-    cursor_enter(p, c, pos);
+    cursor_enter<LOOP>(p, c, pos, n_steps);
   }
   return false;
 }
 
 // The persistent kernel's producer: feeds the ring in schedule order with bulk copies (at most
-// p.inflight outstanding, p.inflight_lm during the LM head). While the ring is full -- the consumers are in a latency-bound stretch
-// (barrier, attention, a small matrix) -- it walks a second cursor ahead and prefetches upcoming
-// stages into L2, paced at about this SM's share of HBM bandwidth and at most l2_lookahead bytes
-// beyond the copies, so that HBM keeps streaming while the ring cannot take more. Later copies of
-// those stages hit L2.
-__device__ __forceinline__ void produce_step(const StepParams& p, Pipe& pp, int pos,
-                                             unsigned long long* trace) {
+// p.inflight outstanding, p.inflight_lm during the LM head). While the ring is full -- the consumers
+// are in a latency-bound stretch (a hand-off, attention, a small matrix) -- it walks a second cursor
+// ahead and prefetches upcoming stages into L2, paced at about this SM's share of HBM bandwidth and
+// at most l2_lookahead bytes beyond the copies, so that HBM keeps streaming while the ring cannot
+// take more. Later copies of those stages hit L2. In the token loop, the copy that reads the slot
+// the previous step wrote first acquires that slot's flag, then orders the acquired view before the
+// bulk copy (a generic-proxy write read by the async proxy).
+template <bool LOOP>
+__device__ __forceinline__ void produce_step(const StepParams& p, Pipe& pp, unsigned long long* trace,
+                                             int n_steps) {
   const uint64_t pol_w = policy_evict_first(), pol_pf = policy_evict_normal();
   // both cursors start before phase 0 with no stage left, so that their first cursor_next enters
   // it (one inlined copy of the cursor code per cursor keeps the producer's code small)
   StageCursor cp{}, pf{};
   cp.k = -1;
   pf.k = -1;
+  int pos_c = p.pos, pos_f = p.pos;
   long long cend = 0, pend = 0;  // stream offsets: end of the current copy, end of prefetched bytes
   uint64_t next_pf = 0;
   bool dead = false;
   const void* src;
   uint32_t bytes;
+  const unsigned* wait = nullptr;
+  unsigned wstamp = 0;
   const volatile int* done = &pp.ms->cons_done;
   int last_k = -1;
-  const int nph = p.m.L * PHASES_PER_LAYER + 1;
-  while (!dead && cursor_next(p, cp, pos, src, bytes)) {
-    if (trace && cp.k != last_k) {  // timeline: the producer moves on to phase cp.k
+  const int nph = phases_per_step(p);
+  while (!dead && cursor_next<LOOP>(p, cp, pos_c, src, bytes, wait, wstamp, n_steps)) {
+    if (trace && cp.k != last_k && cp.k < nph) {  // timeline (first step): the producer moves on to phase cp.k
       const uint64_t t = globaltimer();
       if (last_k >= 0) *trace_at(trace, p, last_k, TR_PROD_END) = t;
       *trace_at(trace, p, cp.k, TR_PROD_BEGIN) = t;
     }
-    last_k = cp.k;
+    if (cp.k < nph) last_k = cp.k;
     cend += bytes;
     const int s = pp.s;
     const uint32_t eb = pp.empty0 + 8u * s;
@@ -201,7 +243,9 @@ __device__ __forceinline__ void produce_step(const StepParams& p, Pipe& pp, int 
           while (pend < (1LL << 62) && pend - cend < p.l2_lookahead) {
             const void* ps;
             uint32_t pb;
-            if (!cursor_next(p, pf, pos, ps, pb)) { pend = 1LL << 62; break; }
+            const unsigned* pw;
+            unsigned pst;
+            if (!cursor_next<LOOP>(p, pf, pos_f, ps, pb, pw, pst, n_steps)) { pend = 1LL << 62; break; }
             const long long start = pend;
             pend += pb;
             if (start >= cend) {
@@ -219,7 +263,26 @@ __device__ __forceinline__ void produce_step(const StepParams& p, Pipe& pp, int 
       }
       if (dead) break;
     }
-    const int infl = min(cp.k == nph - 1 ? p.inflight_lm : pp.inflight, pp.stages);  // <= ring
+    if constexpr (LOOP) {
+      if (wait) {
+        // bounded: the writer published the flag a step ago, so this normally passes at once
+        if (ld_acquire(wait) != wstamp) {
+          const uint64_t t0 = globaltimer();
+          while (ld_acquire(wait) != wstamp) {
+            if (*done) { dead = true; break; }
+            if ((long long)(globaltimer() - t0) > pp.timeout) {
+              dead = true;
+              raise_error(pp.err, pp.err_host, EW_TIMEOUT);
+              break;
+            }
+          }
+          if (dead) break;
+        }
+        fence_proxy_async_global();
+      }
+    }
+    const int klocal = LOOP ? cp.klocal : cp.k;
+    const int infl = min(klocal == nph - 1 ? p.inflight_lm : pp.inflight, pp.stages);  // <= ring
     if (infl > 0 && pp.it >= (uint32_t)infl) {
       const int k = infl;
       const int s2 = s >= k ? s - k : s - k + pp.stages;
@@ -240,13 +303,14 @@ __device__ __forceinline__ void produce_step(const StepParams& p, Pipe& pp, int 
 
 // Consumer side of one attention phase (every unit this CTA owns). Separate from the GEMV phase so
 // that each gets its own register allocation; the pipe state goes in and comes back by value.
+template <bool LOOP>
 __device__ __forceinline__ bool consume_attn_phase(const StepParams& p, Pipe& pp, int layer, int pos,
-                                                   int tid, int k, unsigned long long* trace) {
+                                                   int tid, int k, unsigned long long* trace, unsigned ep) {
   unsigned long long* tr_ready = trace_at(trace, p, k, TR_READY);
   if (tr_ready && tid == 0) *tr_ready = globaltimer();
   // the attention scratch shares shared memory with the row results the QKV epilogue still reads
   named_sync(BAR_CONS, NCT);
-  const AttnArgs A = step_attn_args(p, layer, pos, k);
+  const AttnArgs A = step_attn_args(p, layer, pos, k, ep, LOOP);
   const AttnSplit sp = attn_split(pos, A.nkv, A.d, p.grid, p.slot_bytes, p.n_chunks_override);
   const int units = A.nkv * sp.nch;
   unsigned long long* tr = trace_at(trace, p, k, 0);  // the first unit of the CTA records sub-steps
@@ -286,8 +350,8 @@ __device__ __forceinline__ void fill_phase_table(const StepParams& p, PhaseTable
 // The plan of a GEMV phase: QKV (RMSNorm prologue, bias), O (+ residual), gate/up (RMSNorm,
 // SwiGLU), down (+ residual) or the LM head (final RMSNorm, logits, argmax).
 //
-// Hand-off buffers without barriers. Phase k writes its results as stamped words with stamp
-// epoch + k; phase k + 1 reads them once they carry that stamp. A buffer is rewritten only by a
+// Hand-off buffers without barriers. Phase k of a step writes its results as stamped words with
+// stamp ep + k (ep: the step's first stamp); phase k + 1 reads them once they carry that stamp. A buffer is rewritten only by a
 // later phase of the same kind (qkv by the next layer's QKV, xa by the next O, act by the next
 // gate/up, xb by the next down; the attention output and partials by the next attention). A CTA
 // that rewrites buffer B in phase k' has, in its own phase k' - 1, read the complete results of
@@ -309,7 +373,8 @@ __device__ __forceinline__ void fill_phase_table(const StepParams& p, PhaseTable
 // at about the cost of the grid barrier this hand-off replaces); the data dependency through the
 // stored values is what orders them.
 __device__ __forceinline__ GemvPlan plan_gemv(const StepParams& p, Pipe& pp, int phase, int layer,
-                                              int k, int token, int tid, const PhaseTable* tab) {
+                                              int k, int token, int tid, const PhaseTable* tab,
+                                              unsigned ep) {
   const Dims& m = p.m;
   GemvPlan pl;
   const LayerDev& L = tab ? tab->layers[layer] : p.layers[layer];
@@ -324,10 +389,10 @@ __device__ __forceinline__ GemvPlan plan_gemv(const StepParams& p, Pipe& pp, int
   }
   pl.src = ActSrc{};
   pl.src.eps = m.eps;
-  // phase k reads the stamped results of phase k - 1 and writes its own with stamp epoch + k
-  pl.src.stamp = p.epoch + (unsigned)(k - 1);
+  // phase k reads the stamped results of phase k - 1 and writes its own with stamp ep + k
+  pl.src.stamp = ep + (unsigned)(k - 1);
   pl.src.check = p.stamp_check;
-  const unsigned own = p.epoch + (unsigned)k;
+  const unsigned own = ep + (unsigned)k;
   const uint16_t* erow = p.embed + (size_t)token * m.H;
   switch (phase) {
     case PH_QKV:
@@ -358,7 +423,7 @@ __device__ __forceinline__ GemvPlan plan_gemv(const StepParams& p, Pipe& pp, int
 }
 
 // Consumer side of one GEMV phase from its plan; false when its input never showed up.
-template <int FMT, int NCHL, int IF>
+template <int FMT, int NCHL, int IF, bool LOOP>
 __device__ __forceinline__ bool run_gemv_phase(const StepParams& p, Pipe& pp, const GemvPlan& pl,
                                                int phase, int tid, int k, unsigned long long* trace) {
   const Dims& m = p.m;
@@ -370,29 +435,107 @@ __device__ __forceinline__ bool run_gemv_phase(const StepParams& p, Pipe& pp, co
   if (!ok) return false;
   if (phase == PH_LM) {
     const Best cb = best_block_reduce(best, pp.ms, tid);
-    argmax_publish(cb, p.best_val, p.best_idx, p.best_bad, p.tickets + m.nkv, p.grid, blockIdx.x,
-                   p.argmax, p.err, p.err_host, pp.ms, tid);
+    if (LOOP) {
+      // token loop: this CTA's best as two stamped words; every CTA combines all of them at the
+      // start of the next step
+      if (tid == 0)
+        st_relaxed_v2u64(p.best_w + 2 * blockIdx.x, stamp_word(cb.v, pl.epi.stamp),
+                         ((uint64_t)pl.epi.stamp << 32) | ((uint64_t)(cb.bad ? 1u : 0u) << 31) |
+                             (uint64_t)(unsigned)(cb.i & 0x7FFFFFFF));
+    } else {
+      argmax_publish(cb, p.best_val, p.best_idx, p.best_bad, p.tickets + m.nkv, p.grid, blockIdx.x,
+                     p.argmax, p.err, p.err_host, pp.ms, tid);
+    }
   }
   return true;
 }
 
+// Token loop: the greedy choice of a step from every CTA's stamped best (the largest logit, the
+// lowest token id among ties, and whether any logit was non-finite), combined by warp 0 and handed
+// to the CTA's consumer threads. Every CTA reads the same slots and applies the same
+// order-independent rule, so all of them reach the same token and the same stop decision with no
+// barrier ("Decoding in tiles", section 5: each lm_head task writes its best candidate to its own
+// slot, and every worker combines all slots at the start of the next step). False when a slot never
+// showed up (the CTA's abort flag is then set).
+__device__ __forceinline__ bool gather_best(const StepParams& p, Pipe& pp, unsigned stamp, int tid, Best& out) {
+  Misc* ms = pp.ms;
+  constexpr int PER = 5;  // slots per lane and batch: one batch covers 160 CTAs
+  if (tid < 32) {
+    Best b{-CUDART_INF_F, 0x7FFFFFFF, 0};
+    for (int c0 = 0; c0 < p.grid; c0 += 32 * PER) {
+      uint64_t w0[PER], w1[PER];
+      unsigned need = 0;
+#pragma unroll
+      for (int e = 0; e < PER; ++e) {
+        const int c = c0 + tid + 32 * e;
+        if (c < p.grid) {
+          const ulonglong2 v = ld_relaxed_v2u64(p.best_w + 2 * c);
+          w0[e] = v.x;
+          w1[e] = v.y;
+          need |= 1u << e;
+        }
+      }
+      unsigned stale = 0;
+#pragma unroll
+      for (int e = 0; e < PER; ++e)
+        if ((need & (1u << e)) && (word_stamp(w0[e]) != stamp || word_stamp(w1[e]) != stamp)) stale |= 1u << e;
+      Poll pl;
+      while (stale && pl.again(pp)) {
+#pragma unroll
+        for (int e = 0; e < PER; ++e) {
+          if (stale & (1u << e)) {
+            const ulonglong2 v = ld_relaxed_v2u64(p.best_w + 2 * (c0 + tid + 32 * e));
+            w0[e] = v.x;
+            w1[e] = v.y;
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < PER; ++e)
+          if ((stale & (1u << e)) && word_stamp(w0[e]) == stamp && word_stamp(w1[e]) == stamp) stale &= ~(1u << e);
+      }
+#pragma unroll
+      for (int e = 0; e < PER; ++e) {
+        if (need & (1u << e)) {
+          const float v = word_value(w0[e]);
+          const int i = (int)((uint32_t)w1[e] & 0x7FFFFFFFu);
+          if (v > b.v || (v == b.v && i < b.i)) { b.v = v; b.i = i; }
+          b.bad |= (int)(((uint32_t)w1[e] >> 31) & 1u);
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xFFFFFFFFu, b.v, o);
+      const int oi = __shfl_xor_sync(0xFFFFFFFFu, b.i, o);
+      const int ob = __shfl_xor_sync(0xFFFFFFFFu, b.bad, o);
+      if (ov > b.v || (ov == b.v && oi < b.i)) { b.v = ov; b.i = oi; }
+      b.bad |= ob;
+    }
+    if (tid == 0) { ms->bv[0] = b.v; ms->bi[0] = b.i; ms->bbad[0] = b.bad; }
+  }
+  named_sync(BAR_CONS, NCT);
+  out = Best{ms->bv[0], ms->bi[0], ms->bbad[0]};
+  const bool ok = !*reinterpret_cast<volatile int*>(&ms->abort);
+  named_sync(BAR_CONS, NCT);  // the slots of ms are free again
+  return ok;
+}
+
 // Phase k: its plan (GEMV phases) and its run.
 __device__ __forceinline__ GemvPlan plan_phase(const StepParams& p, Pipe& pp, int k, int token,
-                                               int tid, const PhaseTable* tab = nullptr) {
+                                               int tid, const PhaseTable* tab, unsigned ep) {
   int phase, layer;
   phase_of(k, p.m.L, phase, layer);
   if (phase == PH_ATTN) return GemvPlan{};
-  return plan_gemv(p, pp, phase, layer, k, token, tid, tab);
+  return plan_gemv(p, pp, phase, layer, k, token, tid, tab, ep);
 }
 
-template <int FMT, int NCHL, int IF>
+template <int FMT, int NCHL, int IF, bool LOOP>
 __device__ __forceinline__ bool run_phase(const StepParams& p, Pipe& pp, const GemvPlan& pl, int k,
-                                          int token, int pos, int tid, unsigned long long* trace) {
-  (void)token;
+                                          int pos, int tid, unsigned long long* trace, unsigned ep) {
   int phase, layer;
   phase_of(k, p.m.L, phase, layer);
-  if (phase == PH_ATTN) return consume_attn_phase(p, pp, layer, pos, tid, k, trace);
-  return run_gemv_phase<FMT, NCHL, IF>(p, pp, pl, phase, tid, k, trace);
+  if (phase == PH_ATTN) return consume_attn_phase<LOOP>(p, pp, layer, pos, tid, k, trace, ep);
+  return run_gemv_phase<FMT, NCHL, IF, LOOP>(p, pp, pl, phase, tid, k, trace);
 }
 
 // Start-of-step decision, identical in every CTA: skip when an earlier step left an error, or when
@@ -414,7 +557,9 @@ __device__ __forceinline__ bool step_prologue(const StepParams& p, int& token, i
   return s_tok[1] == 0;
 }
 
-template <int FMT, int NCHL, bool TRACE>
+// LOOP: the instance that runs the token loop (n_steps decode steps per launch); the single-step
+// instance carries none of its state, which keeps the int4 consumers' registers free of spills.
+template <int FMT, int NCHL, bool TRACE, bool LOOP>
 __global__ void __launch_bounds__(NTHREADS_MEGA, 1) decode_megakernel(const __grid_constant__ StepParams p) {
   unsigned long long* const trace = TRACE ? p.trace : nullptr;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -425,26 +570,74 @@ __global__ void __launch_bounds__(NTHREADS_MEGA, 1) decode_megakernel(const __gr
   pp.inflight = p.inflight;
   pipe_setup(pp);
   int token = 0;
-  const int pos = p.pos;
-  if (!step_prologue(p, token, pos, s_tok)) return;
-  const int nph = p.m.L * PHASES_PER_LAYER + 1;
+  if (!step_prologue(p, token, p.pos, s_tok)) return;
+  const int nph = phases_per_step(p);
   const int tid = threadIdx.x;
   if (tid >= NCT) {
     reg_dealloc<FMT ? REG_PRODUCER_INT4 : REG_PRODUCER>();
-    if (tid == NCT) produce_step(p, pp, pos, trace);
+    if (tid == NCT) produce_step<LOOP>(p, pp, trace, LOOP ? p.n_steps : 1);
   } else {
     reg_alloc<FMT ? REG_CONSUMER_INT4 : REG_CONSUMER>();
     // no grid barrier: each phase waits, inside its input fetch, for the stamps of the results it
-    // reads, so a CTA starts a phase as soon as its own inputs are complete
+    // reads, so a CTA starts a phase as soon as its own inputs are complete. With n_steps > 1 the
+    // steps follow one another in this launch ("Decoding in tiles", section 5, Figure 10: one
+    // launch decodes consecutive tokens, greedy selection inside the kernel); stamps keep rising
+    // across steps, so a step needs no barrier either.
     fill_phase_table(p, s_tab, tid);
     named_sync(BAR_CONS, NCT);
-    for (int k = 0; k < nph; ++k) {
-      if (unsigned long long* t = trace_at(trace, p, k, TR_START)) if (tid == 0) *t = globaltimer();
-      const GemvPlan plan = plan_phase(p, pp, k, token, tid, &s_tab);
-      const bool ok = run_phase<FMT, NCHL, 4>(p, pp, plan, k, token, pos, tid, trace);
-      if (unsigned long long* t = trace_at(trace, p, k, TR_END)) if (tid == 0) *t = globaltimer();
+    int done_steps = 0;
+    const int n_steps = LOOP ? p.n_steps : 1;
+    for (int s = 0; s < n_steps; ++s) {
+      const unsigned ep = step_epoch(p, s);
+      const int pos = p.pos + s;
+      if (LOOP && s > 0) {  // the previous step's choice is this step's token
+        Best b;
+        if (!gather_best(p, pp, step_epoch(p, s - 1) + (unsigned)(nph - 1), tid, b)) break;
+        const int tk = b.bad ? -1 : b.i;
+        if (blockIdx.x == 0 && tid == 0) {
+          p.tokens_out[s - 1] = tk;
+          if (b.bad) raise_error(p.err, p.err_host, EW_NONFINITE);
+        }
+        done_steps = s;
+        if (b.bad || tk == p.eos) break;  // the same decision in every CTA
+        token = tk;
+      }
+      unsigned long long* tr = s == 0 ? trace : nullptr;  // the timeline records the first step
+      bool ok = true;
+      for (int k = 0; k < nph && ok; ++k) {
+        if (unsigned long long* t = trace_at(tr, p, k, TR_START)) if (tid == 0) *t = globaltimer();
+        const GemvPlan plan = plan_phase(p, pp, k, token, tid, &s_tab, ep);
+        ok = run_phase<FMT, NCHL, 4, LOOP>(p, pp, plan, k, pos, tid, tr, ep);
+        if (unsigned long long* t = trace_at(tr, p, k, TR_END)) if (tid == 0) *t = globaltimer();
+      }
       if (!ok) break;
+      if (LOOP && s + 1 < n_steps) {
+        // the next step streams slot pos of every layer with bulk copies from other CTAs: the CTA
+        // that wrote it for KV head j (the owner of the chunk holding pos) makes the step's K/V
+        // writes visible at gpu scope and publishes the step's first stamp for j. Done here, after
+        // the LM head's results, the fence delays neither a layer's hand-offs nor the choice.
+        const AttnSplit sp = attn_split(pos, p.m.nkv, p.m.d, p.grid, p.slot_bytes, p.n_chunks_override);
+        const int cpos = pos / sp.cl;
+        bool owner = false;
+        for (int j = 0; j < p.m.nkv; ++j) owner |= (j * sp.nch + cpos) % p.grid == (int)blockIdx.x;
+        if (owner) {
+          fence_acq_rel_gpu();
+          named_sync(BAR_CONS, NCT);
+          if (tid < p.m.nkv && (tid * sp.nch + cpos) % p.grid == (int)blockIdx.x) st_relaxed_u32(p.kvflag + tid, ep);
+        }
+      }
+      if (s == n_steps - 1) {
+        done_steps = s + 1;
+        if (LOOP && blockIdx.x == 0) {  // the last step's choice, recorded by CTA 0
+          Best b;
+          if (gather_best(p, pp, ep + (unsigned)(nph - 1), tid, b) && tid == 0) {
+            p.tokens_out[s] = b.bad ? -1 : b.i;
+            if (b.bad) raise_error(p.err, p.err_host, EW_NONFINITE);
+          }
+        }
+      }
     }
+    if (LOOP && blockIdx.x == 0 && tid == 0 && p.count_out) *p.count_out = done_steps;
     if (tid == 0) *reinterpret_cast<volatile int*>(&pp.ms->cons_done) = 1;
   }
   __syncthreads();
@@ -477,8 +670,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) decode_phase_kernel(const __grid_
     named_sync(BAR_CONS, NCT);
     if (!*reinterpret_cast<volatile int*>(&pp.ms->exit_now)) {
       const int token = p.step_dev[0], pos = p.step_dev[1];
-      const GemvPlan plan = plan_phase(p, pp, k, token, tid);  // after the wait: reads x of the previous kernel
-      (void)run_phase<FMT, NCHL, 4>(p, pp, plan, k, token, pos, tid, p.trace);
+      // after the wait: reads x of the previous kernel
+      const GemvPlan plan = plan_phase(p, pp, k, token, tid, nullptr, p.epoch);
+      (void)run_phase<FMT, NCHL, 4, false>(p, pp, plan, k, pos, tid, p.trace, p.epoch);
     }
     named_sync(BAR_CONS, NCT);
     if (tid == 0) *reinterpret_cast<volatile int*>(&pp.ms->cons_done) = 1;
@@ -488,19 +682,23 @@ __global__ void __launch_bounds__(NTHREADS, 2) decode_phase_kernel(const __grid_
 
 
 // The instances one translation unit provides for its weight format (see mega_bf16.cu and
-// mega_int4.cu): nchl is 4, 6 or 8.
+// mega_int4.cu): nchl is 4, 6 or 8; kind 0 the persistent kernel, 1 the same recording a timeline,
+// 2 the per-phase kernel, 3 the persistent kernel with the token loop.
 #define TINFER_MEGA_INSTANCES(FMT, NAME)                                                        \
   const void* NAME(int nchl, int kind) {                                                        \
     switch (nchl * 4 + kind) {                                                                  \
-      case 16: return reinterpret_cast<const void*>(&decode_megakernel<FMT, 4, false>);         \
-      case 17: return reinterpret_cast<const void*>(&decode_megakernel<FMT, 4, true>);          \
+      case 16: return reinterpret_cast<const void*>(&decode_megakernel<FMT, 4, false, false>);  \
+      case 17: return reinterpret_cast<const void*>(&decode_megakernel<FMT, 4, true, false>);   \
       case 18: return reinterpret_cast<const void*>(&decode_phase_kernel<FMT, 4>);              \
-      case 24: return reinterpret_cast<const void*>(&decode_megakernel<FMT, 6, false>);         \
-      case 25: return reinterpret_cast<const void*>(&decode_megakernel<FMT, 6, true>);          \
+      case 19: return reinterpret_cast<const void*>(&decode_megakernel<FMT, 4, false, true>);   \
+      case 24: return reinterpret_cast<const void*>(&decode_megakernel<FMT, 6, false, false>);  \
+      case 25: return reinterpret_cast<const void*>(&decode_megakernel<FMT, 6, true, false>);   \
       case 26: return reinterpret_cast<const void*>(&decode_phase_kernel<FMT, 6>);              \
-      case 32: return reinterpret_cast<const void*>(&decode_megakernel<FMT, 8, false>);         \
-      case 33: return reinterpret_cast<const void*>(&decode_megakernel<FMT, 8, true>);          \
+      case 27: return reinterpret_cast<const void*>(&decode_megakernel<FMT, 6, false, true>);   \
+      case 32: return reinterpret_cast<const void*>(&decode_megakernel<FMT, 8, false, false>);  \
+      case 33: return reinterpret_cast<const void*>(&decode_megakernel<FMT, 8, true, false>);   \
       case 34: return reinterpret_cast<const void*>(&decode_phase_kernel<FMT, 8>);              \
+      case 35: return reinterpret_cast<const void*>(&decode_megakernel<FMT, 8, false, true>);   \
       default: return nullptr;                                                                  \
     }                                                                                           \
   }

@@ -123,6 +123,12 @@ __device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
 __device__ __forceinline__ void st_relaxed_v2u64(uint64_t* p, uint64_t a, uint64_t b) {
   asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
 }
+__device__ __forceinline__ void st_relaxed_u32(unsigned* p, unsigned v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Makes this thread's earlier writes (and, cumulatively, those ordered before it by a CTA barrier)
+// visible at gpu scope before its later ones.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 __device__ __forceinline__ int ld_volatile_int(const int* p) {
   int v;
   asm volatile("ld.volatile.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");

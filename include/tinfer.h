@@ -141,6 +141,21 @@ tinfer_status tinfer_decode_step_dev(tinfer_ctx* ctx, const int32_t* token_dev, 
 tinfer_status tinfer_generate(tinfer_ctx* ctx, int32_t first_token, int32_t pos0, int32_t n_steps,
                               void* stream, int32_t* tokens_host);
 
+/* Greedy generation in one launch ("Decoding in tiles", section 5, Figure 10: one cooperative
+ * launch decodes consecutive tokens with greedy selection inside the kernel). Step k (k in
+ * [0, n_steps)) runs at position pos0 + k with token first_token for k = 0 and step k - 1's choice
+ * after that; tokens_dev (device int32 [n_steps]) receives every step's choice (-1 for a step with a
+ * non-finite logit, which also sets TINFER_ERR_NONFINITE and ends the run). When eos_token >= 0 the
+ * run ends after the step that chose it. count_dev (device int32 [1], may be NULL) receives the
+ * number of steps completed. Asynchronous on `stream`; slots [pos0, pos0 + count) of the KV cache are
+ * written. Host checks: n_steps >= 1, pos0 + n_steps <= max_ctx, first_token and eos_token in range
+ * (eos_token may be -1), 4-byte aligned outputs; else TINFER_ERR_INVALID_ARG. In graph mode the
+ * steps are separate graph launches chained on the device (eos_token must be -1 and count_dev NULL,
+ * else TINFER_ERR_UNSUPPORTED). */
+tinfer_status tinfer_generate_dev(tinfer_ctx* ctx, int32_t first_token, int32_t pos0, int32_t n_steps,
+                                  int32_t eos_token, void* stream, int32_t* tokens_dev,
+                                  int32_t* count_dev);
+
 /* Waits for all work of the context, then returns and clears the device error word (TINFER_OK if
  * none): TINFER_ERR_NONFINITE for a non-finite logit, TINFER_ERR_TIMEOUT for a device wait that ran
  * out, TINFER_ERR_INVALID_ARG for an out-of-range device token ("Decoding in tiles", section 5:
