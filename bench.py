@@ -271,6 +271,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-loop", action="store_true", help="skip the in-kernel token loop measurement")
+    ap.add_argument("--ffn-split", action="store_true",
+                    help="the column-split down projection variant (bf16 workloads, persistent kernel)")
     ap.add_argument("--no-read-probe", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=0, help="steps of the e2e run (default: the workload's)")
     args = ap.parse_args()
@@ -286,7 +288,7 @@ def main():
     rank, local, world, dist = dist_setup(args.gpus)
     torch.cuda.set_device(local)
     T.build()
-    c = synth.config(args.config)
+    c = synth.config(args.config, **({"ffn_split": True} if args.ffn_split else {}))
     w = synth.make_model(c, seed=0)
     P = c["prefill"] + c["prompt"]
     S = c["steps"]
@@ -430,7 +432,8 @@ def main():
         "dtype": "bf16" if c["weight_format"] == "bf16" else "int4",
         "data": "synthetic",
         "config": workload_config(c, world),
-        "exec_mode": "persistent megakernel" if main_mode == "mega" else "cuda graph",
+        "exec_mode": ("persistent megakernel" if main_mode == "mega" else "cuda graph") +
+                     (", column-split down projection" if args.ffn_split else ""),
         "positions_timed": f"{P}..{P + min(steps, S) - 1}" + (f", cycled {steps / S:.1f} times" if steps > S else ""),
         "bytes_per_step": bytes_step,
         "floor_frac_nominal_8tbs": achieved / NOMINAL_HBM_GBS,

@@ -45,7 +45,7 @@ class tinfer_config(ctypes.Structure):
         "n_layers", "hidden", "n_heads", "n_kv_heads", "head_dim", "ffn", "vocab", "max_ctx")] + [
         ("rope_theta", ctypes.c_double), ("rms_eps", ctypes.c_double)] + [
         (n, ctypes.c_int) for n in ("weight_format", "group_size", "scale_dtype", "tied_embeddings",
-                                    "qkv_bias", "exec_mode")]
+                                    "qkv_bias", "exec_mode", "ffn_split")]
 
 
 class tinfer_layer_src(ctypes.Structure):
@@ -260,6 +260,7 @@ def make_config(c: dict, exec_mode: int = TINFER_MEGAKERNEL) -> tinfer_config:
     cfg.tied_embeddings = 1 if c.get("tied") else 0
     cfg.qkv_bias = 1 if c.get("qkv_bias") else 0
     cfg.exec_mode = int(exec_mode)
+    cfg.ffn_split = 1 if c.get("ffn_split") else 0
     return cfg
 
 

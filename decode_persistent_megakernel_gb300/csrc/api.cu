@@ -149,6 +149,12 @@ tinfer_status tinfer_check_config(const tinfer_config* c) {
   if (!(c->rope_theta > 0.0) || !(c->rms_eps >= 0.0)) return TINFER_ERR_INVALID_ARG;
   if (c->n_heads % c->n_kv_heads != 0 || c->head_dim % 2 != 0) return TINFER_ERR_INVALID_ARG;
   if (c->exec_mode != TINFER_MEGAKERNEL && c->exec_mode != TINFER_GRAPH) return TINFER_ERR_INVALID_ARG;
+  if (c->ffn_split != 0 && c->ffn_split != 1) return TINFER_ERR_INVALID_ARG;
+  // the column-split down projection: bf16 rows of hidden outputs, at most two 8-output chunks per
+  // consumer thread; its in-kernel reduce needs the co-resident CTAs of the persistent launch
+  if (c->ffn_split && (c->weight_format != TINFER_BF16 || c->exec_mode != TINFER_MEGAKERNEL ||
+                       c->hidden % 8 != 0 || c->hidden / 8 > 2 * NCT))
+    return TINFER_ERR_UNSUPPORTED;
   if (c->n_layers > MAX_LAYERS) return TINFER_ERR_UNSUPPORTED;
   if (c->weight_format != TINFER_BF16 && c->weight_format != TINFER_INT4) return TINFER_ERR_INVALID_ARG;
   if (c->n_heads / c->n_kv_heads > G_MAX || c->head_dim % 8 != 0 || c->head_dim > D_MAX)
@@ -236,7 +242,12 @@ tinfer_status tinfer_pack_layer(const tinfer_config* c, const tinfer_layer_src* 
   TRY(pack_one(f, g, src->wo, src->so, H, nq * d, b + L.off_o, 1, 0, st));
   TRY(pack_one(f, g, src->wg, src->sg, F, H, b + L.off_gu, 2, 0, st));
   TRY(pack_one(f, g, src->wu, src->su, F, H, b + L.off_gu, 2, 1, st));
-  TRY(pack_one(f, g, src->wd, src->sd, H, F, b + L.off_down, 1, 0, st));
+  if (c->ffn_split) {  // Wd^T: row f holds the weights of ffn input f for every hidden output
+    if (!src->wd) return TINFER_ERR_INVALID_ARG;
+    TRY_CUDA(launch_transpose_u16((const uint16_t*)src->wd, H, F, (uint16_t*)(b + L.off_down), st));
+  } else {
+    TRY(pack_one(f, g, src->wd, src->sd, H, F, b + L.off_down, 1, 0, st));
+  }
   if (!src->g1 || !src->g2) return TINFER_ERR_INVALID_ARG;
   TRY_CUDA(launch_bf16_to_f32((const uint16_t*)src->g1, (float*)(b + L.off_g1), H, st));
   TRY_CUDA(launch_bf16_to_f32((const uint16_t*)src->g2, (float*)(b + L.off_g2), H, st));
@@ -265,7 +276,12 @@ tinfer_status tinfer_unpack_layer(const tinfer_config* c, const void* packed_dev
   TRY(unpack_one(f, g, dst->wo, dst->so, H, nq * d, b + L.off_o, 1, 0, st));
   TRY(unpack_one(f, g, dst->wg, dst->sg, F, H, b + L.off_gu, 2, 0, st));
   TRY(unpack_one(f, g, dst->wu, dst->su, F, H, b + L.off_gu, 2, 1, st));
-  TRY(unpack_one(f, g, dst->wd, dst->sd, H, F, b + L.off_down, 1, 0, st));
+  if (c->ffn_split) {
+    if (!dst->wd) return TINFER_ERR_INVALID_ARG;
+    TRY_CUDA(launch_transpose_u16((const uint16_t*)(b + L.off_down), F, H, (uint16_t*)dst->wd, st));
+  } else {
+    TRY(unpack_one(f, g, dst->wd, dst->sd, H, F, b + L.off_down, 1, 0, st));
+  }
   if (!dst->g1 || !dst->g2) return TINFER_ERR_INVALID_ARG;
   TRY_CUDA(launch_f32_to_bf16((const float*)(b + L.off_g1), (uint16_t*)dst->g1, H, st));
   TRY_CUDA(launch_f32_to_bf16((const float*)(b + L.off_g2), (uint16_t*)dst->g2, H, st));
@@ -344,6 +360,7 @@ tinfer_status tinfer_create(const tinfer_config* c, const tinfer_weights* w, voi
   if ((st = cu(megakernel_occupancy(&occ, x->smem_mega, c->weight_format, nchl))) != TINFER_OK) return fail(st);
   if (occ < 1) return fail(TINFER_ERR_UNSUPPORTED);
   const int grid = x->num_sms;  // one persistent CTA per SM (co-residency: cooperative launch)
+  if (c->ffn_split && grid > 256) return fail(TINFER_ERR_UNSUPPORTED);  // partials per reduce lane
   {
     // row results of one GEMV phase must fit the per-CTA shared-memory buffer
     const int f = c->weight_format;
@@ -376,6 +393,7 @@ tinfer_status tinfer_create(const tinfer_config* c, const tinfer_weights* w, voi
   const size_t o_bv = take((size_t)grid * 4), o_bi = take((size_t)grid * 4), o_bb = take((size_t)grid * 4);
   const size_t o_err = take(4), o_step = take(2 * 4), o_gen = take(2 * 4), o_am = take(4);
   const size_t o_bw = take((size_t)grid * 16), o_kvf = take((size_t)c->n_layers * nkv * 4);
+  const size_t o_pf = take(c->ffn_split ? (size_t)grid * H * 8 : 8);
   if ((st = cu(cudaMalloc(&x->scratch, off))) != TINFER_OK) return fail(st);
   if ((st = cu(cudaMemset(x->scratch, 0, off))) != TINFER_OK) return fail(st);
   uint8_t* s = (uint8_t*)x->scratch;
@@ -414,6 +432,7 @@ tinfer_status tinfer_create(const tinfer_config* c, const tinfer_weights* w, voi
   m.rb_lm = H * 2;
   m.qkv_rows = qkv_rows;
   m.nchl = nchl;
+  m.ffn_split = c->ffn_split;
   for (int l = 0; l < c->n_layers; ++l) p.layers[l] = ld[l];
   p.embed = (const uint16_t*)w->embed;
   p.lm_head = (const uint16_t*)w->lm_head;
@@ -423,6 +442,7 @@ tinfer_status tinfer_create(const tinfer_config* c, const tinfer_weights* w, voi
   p.rope = x->rope_dev;
   p.xa = (uint64_t*)(s + o_xa); p.xb = (uint64_t*)(s + o_xb); p.qkv = (uint64_t*)(s + o_qkv);
   p.attn = (uint64_t*)(s + o_attn); p.act = (uint64_t*)(s + o_act);
+  p.part_ffn = (uint64_t*)(s + o_pf);
   p.epoch = 1;  // the buffers start zeroed: stamp 0 is never expected
   p.stamp_check = c->exec_mode == TINFER_MEGAKERNEL;
   p.part_m = (float*)(s + o_pm); p.part_l = (float*)(s + o_pl); p.part_o = (float*)(s + o_po);

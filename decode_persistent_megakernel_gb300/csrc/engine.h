@@ -66,6 +66,7 @@ struct Dims {
   int rb_lm;              // bf16 LM head row bytes (2 * hidden)
   int qkv_rows;           // (nq + 2 nkv) * d
   int nchl;               // bf16 GEMV instance of the step kernels: 16-byte chunks per lane (4, 6, 8)
+  int ffn_split;          // down projection split by columns (Wd stored transposed: [F][H])
 };
 
 // Everything one step needs; passed by value to every kernel (16-byte multiple: copied to shared
@@ -87,6 +88,7 @@ struct __align__(16) StepParams {
   uint64_t* qkv;           // [qkv_rows]
   uint64_t* attn;          // [nq * d]
   uint64_t* act;           // [F]
+  uint64_t* part_ffn;      // [grid][H] column-split down projection: per-CTA partial sums (stamped)
   unsigned epoch;          // stamps of this launch: phase k writes epoch + k
   int stamp_check;         // readers wait for the stamp (persistent kernel); 0: stream order suffices
   float* part_m;           // [nq][nch_cap]      (per-phase kernels: ticket merge)

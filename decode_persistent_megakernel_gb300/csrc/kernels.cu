@@ -122,6 +122,22 @@ __global__ void unpack_rows_kernel(const uint8_t* src, int src_rb, int src_step,
   }
 }
 
+// out[c][r] = in[r][c] for 16-bit elements (the packer's transposed down projection), 32 x 32
+// tiles through shared memory.
+__global__ void transpose_u16_kernel(const uint16_t* in, int rows, int cols, uint16_t* out) {
+  __shared__ uint16_t t[32][33];
+  const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int r = r0 + i, c = c0 + threadIdx.x;
+    if (r < rows && c < cols) t[i][threadIdx.x] = in[(size_t)r * cols + c];
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int c = c0 + i, r = r0 + threadIdx.x;
+    if (r < rows && c < cols) out[(size_t)c * rows + r] = t[threadIdx.x][i];
+  }
+}
+
 __global__ void bf16_to_f32_kernel(const uint16_t* in, float* out, int n) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
     out[i] = __uint_as_float((uint32_t)in[i] << 16);
@@ -136,7 +152,8 @@ __global__ void f32_to_bf16_kernel(const float* in, uint16_t* out, int n) {
 // ------------------------------------------------------------------------------ launch wrappers
 
 // kernel instances of mega_bf16.cu / mega_int4.cu; kind 0: persistent kernel, 1: persistent kernel
-// recording a timeline, 2: per-phase kernel, 3: persistent kernel with the token loop
+// recording a timeline, 2: per-phase kernel, 3: persistent kernel with the token loop, 4: persistent
+// kernel with the column-split down projection (bf16)
 const void* step_kernel_bf16(int nchl, int kind);
 const void* step_kernel_int4(int nchl, int kind);
 static const void* step_fn(int fmt, int nchl, int kind) {
@@ -144,7 +161,7 @@ static const void* step_fn(int fmt, int nchl, int kind) {
 }
 
 cudaError_t launch_megakernel(const StepParams& p, size_t smem, cudaStream_t st) {
-  const void* fn = step_fn(p.m.fmt, p.m.nchl, p.n_steps > 1 ? 3 : p.trace ? 1 : 0);
+  const void* fn = step_fn(p.m.fmt, p.m.nchl, p.m.ffn_split ? 4 : p.n_steps > 1 ? 3 : p.trace ? 1 : 0);
   if (!fn) return cudaErrorInvalidDeviceFunction;
   void* args[] = {const_cast<StepParams*>(&p)};
   return cudaLaunchCooperativeKernel(fn, dim3(p.grid), dim3(NTHREADS_MEGA), args, smem, st);
@@ -211,8 +228,10 @@ static cudaError_t raise_limit(const void* fn, size_t bytes) {
   return cudaSuccess;
 }
 cudaError_t set_smem_mega(size_t b, int fmt, int nchl) {
-  for (int kind : {0, 1, 3}) {
-    const cudaError_t e = raise_limit(step_fn(fmt, nchl, kind), b);
+  for (int kind : {0, 1, 3, 4}) {
+    const void* fn = step_fn(fmt, nchl, kind);
+    if (!fn && kind == 4) continue;  // no column-split instance for int4
+    const cudaError_t e = raise_limit(fn, b);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -247,6 +266,11 @@ cudaError_t launch_unpack_rows(const uint8_t* src, int src_rb, int src_step, int
   if (rows <= 0) return cudaSuccess;
   unpack_rows_kernel<<<rows < 4096 ? rows : 4096, 128, 0, st>>>(src, src_rb, src_step, src_first, rows,
                                                               w, w_bytes, s, s_bytes);
+  return cudaGetLastError();
+}
+cudaError_t launch_transpose_u16(const uint16_t* in, int rows, int cols, uint16_t* out, cudaStream_t st) {
+  if (rows <= 0 || cols <= 0) return cudaSuccess;
+  transpose_u16_kernel<<<dim3((cols + 31) / 32, (rows + 31) / 32), dim3(32, 8), 0, st>>>(in, rows, cols, out);
   return cudaGetLastError();
 }
 cudaError_t launch_bf16_to_f32(const uint16_t* in, float* out, int n, cudaStream_t st) {

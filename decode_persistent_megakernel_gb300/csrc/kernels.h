@@ -66,6 +66,7 @@ cudaError_t launch_pack_rows(uint8_t* dst, int dst_rb, int dst_step, int dst_fir
 cudaError_t launch_unpack_rows(const uint8_t* src, int src_rb, int src_step, int src_first, int rows,
                                uint8_t* w, int w_bytes, uint8_t* s, int s_bytes, cudaStream_t st);
 cudaError_t launch_bf16_to_f32(const uint16_t* in, float* out, int n, cudaStream_t st);
+cudaError_t launch_transpose_u16(const uint16_t* in, int rows, int cols, uint16_t* out, cudaStream_t st);
 cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, int n, cudaStream_t st);
 
 }  // namespace tinfer

@@ -36,7 +36,11 @@ __device__ __forceinline__ GemvDesc phase_gemv(const StepParams& p, int phase, i
     case PH_QKV: g.w = L.qkv; g.rows = m.qkv_rows; g.cols = m.H; g.rb = m.rb_h; break;
     case PH_O: g.w = L.o; g.rows = m.H; g.cols = m.nq * m.d; g.rb = m.rb_qd; break;
     case PH_GU: g.w = L.gu; g.rows = 2 * m.F; g.cols = m.H; g.rb = m.rb_h; g.quantum = 2; break;
-    case PH_DOWN: g.w = L.down; g.rows = m.H; g.cols = m.F; g.rb = m.rb_f; break;
+    case PH_DOWN:
+      g.w = L.down;
+      if (m.ffn_split) { g.rows = m.F; g.cols = m.H; g.rb = m.rb_h; }  // Wd^T, this CTA's ffn inputs
+      else { g.rows = m.H; g.cols = m.F; g.rb = m.rb_f; }
+      break;
     default:
       g.w = reinterpret_cast<const uint8_t*>(p.lm_head);
       g.rows = m.V; g.cols = m.H; g.rb = m.rb_lm; g.fmt = 0;
@@ -411,7 +415,8 @@ __device__ __forceinline__ GemvPlan plan_gemv(const StepParams& p, Pipe& pp, int
       break;
     case PH_DOWN:
       pl.src.xw = p.act; pl.src.n = m.F;
-      pl.epi = Epi{EK_RESIDUAL, p.xb, nullptr, p.xa, own, EF_OUT_STAMPED | EF_RES_STAMPED};
+      pl.epi = Epi{m.ffn_split ? EK_COLSPLIT : EK_RESIDUAL, p.xb, nullptr, p.xa, own,
+                   EF_OUT_STAMPED | EF_RES_STAMPED};
       break;
     default:
       pl.src.xw = p.xb; pl.src.gb = p.final_norm; pl.src.n = m.H;
@@ -423,12 +428,20 @@ __device__ __forceinline__ GemvPlan plan_gemv(const StepParams& p, Pipe& pp, int
 }
 
 // Consumer side of one GEMV phase from its plan; false when its input never showed up.
-template <int FMT, int NCHL, int IF, bool LOOP>
+template <int FMT, int NCHL, int IF, bool LOOP, bool SPLIT>
 __device__ __forceinline__ bool run_gemv_phase(const StepParams& p, Pipe& pp, const GemvPlan& pl,
                                                int phase, int tid, int k, unsigned long long* trace) {
   const Dims& m = p.m;
   unsigned long long* tr_ready = trace_at(trace, p, k, TR_READY);
   Best best{-CUDART_INF_F, 0x7FFFFFFF, 0};
+  if constexpr (FMT == 0 && SPLIT) {
+    if (pl.epi.kind == EK_COLSPLIT) {
+    // the output rows of the reduce are the O phase's split of the hidden rows (their residual
+    // rows are this CTA's own)
+      const RowSplit ro = row_split(GemvDesc{nullptr, m.H, m.F, 0, 0, 0, 0, 1}, blockIdx.x, p.grid, p.slot_bytes);
+      return colsplit_down(pp, pl, ro, p.part_ffn, p.grid, tid);
+    }
+  }
   // int4 models stream their linears as int4 and the LM head as bf16; bf16 models need one format
   const bool ok = (FMT == 1 && pl.g.fmt == 1) ? gemv_rows<1, 2>(pp, pl, best, tid, tr_ready)
                                               : gemv_rows<0, NCHL, IF>(pp, pl, best, tid, tr_ready);
@@ -529,13 +542,13 @@ __device__ __forceinline__ GemvPlan plan_phase(const StepParams& p, Pipe& pp, in
   return plan_gemv(p, pp, phase, layer, k, token, tid, tab, ep);
 }
 
-template <int FMT, int NCHL, int IF, bool LOOP>
+template <int FMT, int NCHL, int IF, bool LOOP, bool SPLIT>
 __device__ __forceinline__ bool run_phase(const StepParams& p, Pipe& pp, const GemvPlan& pl, int k,
                                           int pos, int tid, unsigned long long* trace, unsigned ep) {
   int phase, layer;
   phase_of(k, p.m.L, phase, layer);
   if (phase == PH_ATTN) return consume_attn_phase<LOOP>(p, pp, layer, pos, tid, k, trace, ep);
-  return run_gemv_phase<FMT, NCHL, IF, LOOP>(p, pp, pl, phase, tid, k, trace);
+  return run_gemv_phase<FMT, NCHL, IF, LOOP, SPLIT>(p, pp, pl, phase, tid, k, trace);
 }
 
 // Start-of-step decision, identical in every CTA: skip when an earlier step left an error, or when
@@ -559,7 +572,10 @@ __device__ __forceinline__ bool step_prologue(const StepParams& p, int& token, i
 
 // LOOP: the instance that runs the token loop (n_steps decode steps per launch); the single-step
 // instance carries none of its state, which keeps the int4 consumers' registers free of spills.
-template <int FMT, int NCHL, bool TRACE, bool LOOP>
+// SPLIT: the instance for the column-split down projection (Dims::ffn_split). Each variant is its
+// own instance because the persistent kernel's speed depends on its code size and registers: the
+// column-split code compiled into the other instances made the Llama-shaped step 13 % slower.
+template <int FMT, int NCHL, bool TRACE, bool LOOP, bool SPLIT = false>
 __global__ void __launch_bounds__(NTHREADS_MEGA, 1) decode_megakernel(const __grid_constant__ StepParams p) {
   unsigned long long* const trace = TRACE ? p.trace : nullptr;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -607,7 +623,7 @@ __global__ void __launch_bounds__(NTHREADS_MEGA, 1) decode_megakernel(const __gr
       for (int k = 0; k < nph && ok; ++k) {
         if (unsigned long long* t = trace_at(tr, p, k, TR_START)) if (tid == 0) *t = globaltimer();
         const GemvPlan plan = plan_phase(p, pp, k, token, tid, &s_tab, ep);
-        ok = run_phase<FMT, NCHL, 4, LOOP>(p, pp, plan, k, pos, tid, tr, ep);
+        ok = run_phase<FMT, NCHL, 4, LOOP, SPLIT>(p, pp, plan, k, pos, tid, tr, ep);
         if (unsigned long long* t = trace_at(tr, p, k, TR_END)) if (tid == 0) *t = globaltimer();
       }
       if (!ok) break;
@@ -672,7 +688,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) decode_phase_kernel(const __grid_
       const int token = p.step_dev[0], pos = p.step_dev[1];
       // after the wait: reads x of the previous kernel
       const GemvPlan plan = plan_phase(p, pp, k, token, tid, nullptr, p.epoch);
-      (void)run_phase<FMT, NCHL, 4, false>(p, pp, plan, k, pos, tid, p.trace, p.epoch);
+      (void)run_phase<FMT, NCHL, 4, false, false>(p, pp, plan, k, pos, tid, p.trace, p.epoch);
     }
     named_sync(BAR_CONS, NCT);
     if (tid == 0) *reinterpret_cast<volatile int*>(&pp.ms->cons_done) = 1;
@@ -683,24 +699,23 @@ __global__ void __launch_bounds__(NTHREADS, 2) decode_phase_kernel(const __grid_
 
 // The instances one translation unit provides for its weight format (see mega_bf16.cu and
 // mega_int4.cu): nchl is 4, 6 or 8; kind 0 the persistent kernel, 1 the same recording a timeline,
-// 2 the per-phase kernel, 3 the persistent kernel with the token loop.
-#define TINFER_MEGA_INSTANCES(FMT, NAME)                                                        \
-  const void* NAME(int nchl, int kind) {                                                        \
-    switch (nchl * 4 + kind) {                                                                  \
-      case 16: return reinterpret_cast<const void*>(&decode_megakernel<FMT, 4, false, false>);  \
-      case 17: return reinterpret_cast<const void*>(&decode_megakernel<FMT, 4, true, false>);   \
-      case 18: return reinterpret_cast<const void*>(&decode_phase_kernel<FMT, 4>);              \
-      case 19: return reinterpret_cast<const void*>(&decode_megakernel<FMT, 4, false, true>);   \
-      case 24: return reinterpret_cast<const void*>(&decode_megakernel<FMT, 6, false, false>);  \
-      case 25: return reinterpret_cast<const void*>(&decode_megakernel<FMT, 6, true, false>);   \
-      case 26: return reinterpret_cast<const void*>(&decode_phase_kernel<FMT, 6>);              \
-      case 27: return reinterpret_cast<const void*>(&decode_megakernel<FMT, 6, false, true>);   \
-      case 32: return reinterpret_cast<const void*>(&decode_megakernel<FMT, 8, false, false>);  \
-      case 33: return reinterpret_cast<const void*>(&decode_megakernel<FMT, 8, true, false>);   \
-      case 34: return reinterpret_cast<const void*>(&decode_phase_kernel<FMT, 8>);              \
-      case 35: return reinterpret_cast<const void*>(&decode_megakernel<FMT, 8, false, true>);   \
-      default: return nullptr;                                                                  \
-    }                                                                                           \
+// 2 the per-phase kernel, 3 the persistent kernel with the token loop, 4 the persistent kernel with
+// the column-split down projection (bf16 only).
+#define TINFER_MEGA_CASES(FMT, N)                                                                \
+  case N * 8 + 0: return reinterpret_cast<const void*>(&decode_megakernel<FMT, N, false, false>); \
+  case N * 8 + 1: return reinterpret_cast<const void*>(&decode_megakernel<FMT, N, true, false>);  \
+  case N * 8 + 2: return reinterpret_cast<const void*>(&decode_phase_kernel<FMT, N>);             \
+  case N * 8 + 3: return reinterpret_cast<const void*>(&decode_megakernel<FMT, N, false, true>);  \
+  case N * 8 + 4: return FMT == 0 ? reinterpret_cast<const void*>(                                \
+                             &decode_megakernel<FMT, N, false, false, FMT == 0>) : nullptr;
+#define TINFER_MEGA_INSTANCES(FMT, NAME)                                                          \
+  const void* NAME(int nchl, int kind) {                                                          \
+    switch (nchl * 8 + kind) {                                                                    \
+      TINFER_MEGA_CASES(FMT, 4)                                                                   \
+      TINFER_MEGA_CASES(FMT, 6)                                                                   \
+      TINFER_MEGA_CASES(FMT, 8)                                                                   \
+      default: return nullptr;                                                                    \
+    }                                                                                             \
   }
 
 }  // namespace tinfer

@@ -383,7 +383,7 @@ __device__ __forceinline__ RowSplit row_split(const GemvDesc& g, int cta, int gr
   return RowSplit{u0 * g.quantum, u1 * g.quantum, stage_rows(g.fmt, g.cols, g.rb, slot, g.quantum)};
 }
 
-enum EpiKind : int { EK_STORE = 0, EK_RESIDUAL = 1, EK_SWIGLU = 2, EK_ARGMAX = 3 };
+enum EpiKind : int { EK_STORE = 0, EK_RESIDUAL = 1, EK_SWIGLU = 2, EK_ARGMAX = 3, EK_COLSPLIT = 4 };
 struct Epi {
   int kind;
   void* out;              // output: plain floats (single operations, logits) or stamped words
@@ -755,6 +755,114 @@ __device__ __forceinline__ bool gemv_rows(Pipe& pp, const GemvPlan& pl, Best& be
     }
   }
   return true;
+}
+
+// The MLP's down projection split by columns ("Decoding in tiles", section 4: each worker
+// multiplies its SwiGLU rows by the matching columns of the down projection, an fp32 partial sum of
+// every output, and an FFN-reduce task sums the partials in a fixed order and adds the residual).
+// pl.g is Wd^T with this CTA's ffn inputs [rs.r0, rs.r1) as rows; their SwiGLU values are this
+// CTA's own results of the gate/up phase (the same split), read from pl.src.xw after a barrier.
+// Thread t accumulates hidden outputs [8 c, 8 c + 8) for chunks c = t, t + NCT (row by row, in
+// order), publishes them as stamped words (the gate/up phase's stamp, which nothing else uses in
+// this mode), and the CTA then reduces its output rows ro over every CTA's partials: sixteen lanes
+// per row, lane s summing the partials of CTAs s, s + 16, ... in order, a fixed xor tree over the
+// sixteen, the residual added last. So the gate/up results never cross CTAs, and the reduce is
+// the only hand-off between the gate/up and the next phase. False when a partial never showed up.
+__device__ __forceinline__ bool colsplit_down(Pipe& pp, const GemvPlan& pl, const RowSplit& ro, uint64_t* part,
+                                           int grid, int tid) {
+  constexpr int CPT = 2;  // 8-output chunks per thread: hidden sizes up to 16 * NCT
+  Misc* ms = pp.ms;
+  const GemvDesc& g = pl.g;
+  const RowSplit& rs = pl.rs;
+  const Epi& epi = pl.epi;
+  const int H = g.cols, nchunk = H / 8, nrows = rs.r1 - rs.r0;
+  const unsigned ps = epi.stamp - 1u;
+  float* act_s = sptr_w<float>(smem_addr(ms->rowv));
+  named_sync(BAR_CONS, NCT);  // the gate/up epilogue has written every SwiGLU value of this CTA
+  for (int t = tid; t < nrows; t += NCT) act_s[t] = word_value(ld_relaxed_u64(pl.src.xw + rs.r0 + t));
+  named_sync(BAR_CONS, NCT);
+  float2 acc[CPT][4];
+#pragma unroll
+  for (int c = 0; c < CPT; ++c)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[c][e] = make_float2(0.f, 0.f);
+  const int lane = tid & 31;
+  for (int s0 = rs.r0; s0 < rs.r1; s0 += rs.nr) {
+    const int nrs = min(rs.nr, rs.r1 - s0);
+    const uint32_t st = cons_acquire(pp);
+#pragma unroll 1
+    for (int i = 0; i < nrs; ++i) {
+      const float a = act_s[s0 - rs.r0 + i];
+      const float2 a2 = make_float2(a, a);
+#pragma unroll
+      for (int c = 0; c < CPT; ++c) {
+        const int ch = tid + c * NCT;
+        if (ch < nchunk) {
+          const uint4 w = lds128(st + (uint32_t)i * g.rb + (uint32_t)ch * 16u);
+          acc[c][0] = fma2(a2, make_float2(bf16_lo(w.x), bf16_hi(w.x)), acc[c][0]);
+          acc[c][1] = fma2(a2, make_float2(bf16_lo(w.y), bf16_hi(w.y)), acc[c][1]);
+          acc[c][2] = fma2(a2, make_float2(bf16_lo(w.z), bf16_hi(w.z)), acc[c][2]);
+          acc[c][3] = fma2(a2, make_float2(bf16_lo(w.w), bf16_hi(w.w)), acc[c][3]);
+        }
+      }
+    }
+    cons_release(pp, lane);
+  }
+  uint64_t* mine = part + (size_t)blockIdx.x * H;
+#pragma unroll
+  for (int c = 0; c < CPT; ++c) {
+    const int ch = tid + c * NCT;
+    if (ch < nchunk) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        st_relaxed_v2u64(mine + ch * 8 + 2 * e, stamp_word(acc[c][e].x, ps), stamp_word(acc[c][e].y, ps));
+    }
+  }
+  // the reduce: two rows per warp and turn (one per half-warp), every lane in every shuffle
+  const int warp = tid >> 5, half = lane >> 4, sub = lane & 15;
+  const int nout = ro.r1 - ro.r0;
+  constexpr int PER = 16;  // partials per lane: grids up to 256 CTAs
+  for (int rb = 2 * warp; rb < nout; rb += 2 * NCW) {
+    const int rr = rb + half;
+    const bool on = rr < nout;
+    const int r = ro.r0 + rr;
+    uint64_t w[PER];
+    unsigned need = 0;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+      const int cta = sub + 16 * e;
+      if (on && cta < grid) {
+        w[e] = ld_relaxed_u64(part + (size_t)cta * H + r);
+        need |= 1u << e;
+      } else {
+        w[e] = 0;
+      }
+    }
+    {
+      unsigned stale = 0;
+#pragma unroll
+      for (int e = 0; e < PER; ++e)
+        if ((need & (1u << e)) && word_stamp(w[e]) != ps) stale |= 1u << e;
+      Poll pl2;
+      while (stale && pl2.again(pp)) {
+#pragma unroll
+        for (int e = 0; e < PER; ++e)
+          if (stale & (1u << e)) w[e] = ld_relaxed_u64(part + (size_t)(sub + 16 * e) * H + r);
+#pragma unroll
+        for (int e = 0; e < PER; ++e)
+          if ((stale & (1u << e)) && word_stamp(w[e]) == ps) stale &= ~(1u << e);
+      }
+    }
+    float v = 0.f;
+#pragma unroll
+    for (int e = 0; e < PER; ++e)
+      if (need & (1u << e)) v += word_value(w[e]);
+#pragma unroll
+    for (int o = 8; o; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    if (on && sub == 0) epi_write(epi, r, residual_at(epi, r) + v);
+  }
+  named_sync(BAR_CONS, NCT);
+  return !*reinterpret_cast<volatile int*>(&ms->abort);
 }
 
 // Dispatch to the instance of the weight format and chunk count per lane (rounded up to even).

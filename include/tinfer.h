@@ -61,6 +61,11 @@ typedef struct {
   int tied_embeddings; /* informational: lm_head may equal embed */
   int qkv_bias;        /* 1: bf16 biases are added to q, k, v before RoPE */
   int exec_mode;       /* TINFER_MEGAKERNEL (one persistent launch per step) or TINFER_GRAPH */
+  int ffn_split;       /* 1: the MLP's down projection split by columns ("Decoding in tiles", section
+                          4, "FFN" and "FFN reduce"): each CTA multiplies its own SwiGLU rows by the
+                          matching columns of Wd and the partial sums are reduced in a fixed order.
+                          The packed layer then stores Wd transposed. bf16 weights and
+                          TINFER_MEGAKERNEL only (else TINFER_ERR_UNSUPPORTED); 0: row-split down. */
 } tinfer_config;
 
 /* Canonical per-layer weights (device pointers), the input of tinfer_pack_layer.
