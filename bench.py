@@ -271,6 +271,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-loop", action="store_true", help="skip the in-kernel token loop measurement")
+    ap.add_argument("--sync", default="stamps", choices=["stamps", "barrier"],
+                    help="how a phase waits for the one before it (persistent kernel)")
     ap.add_argument("--ffn-split", action="store_true",
                     help="the column-split down projection variant (bf16 workloads, persistent kernel)")
     ap.add_argument("--no-read-probe", action="store_true")
@@ -301,6 +303,8 @@ def main():
     first = int(synth.make_tokens(c, 1)[0])
     for name, mode in modes:
         eng = T.Engine(c, w, mode, kv=(K, V))
+        if mode == T.TINFER_MEGAKERNEL and args.sync == "barrier":
+            assert T.tinfer_set_schedule(eng.ctx, T.TINFER_S_SYNC, T.TINFER_SYNC_GRID_BARRIER) == 0
         # warm-up, then a short calibration: the timed region covers at least MIN_TIMED_S of steps
         # whatever --steps asks for (so that the clock sampler sees the run); the line reports the
         # steps actually timed
@@ -433,7 +437,8 @@ def main():
         "data": "synthetic",
         "config": workload_config(c, world),
         "exec_mode": ("persistent megakernel" if main_mode == "mega" else "cuda graph") +
-                     (", column-split down projection" if args.ffn_split else ""),
+                     (", column-split down projection" if args.ffn_split else "") +
+                     (", grid barrier before every phase" if args.sync == "barrier" else ""),
         "positions_timed": f"{P}..{P + min(steps, S) - 1}" + (f", cycled {steps / S:.1f} times" if steps > S else ""),
         "bytes_per_step": bytes_step,
         "floor_frac_nominal_8tbs": achieved / NOMINAL_HBM_GBS,

@@ -394,6 +394,7 @@ tinfer_status tinfer_create(const tinfer_config* c, const tinfer_weights* w, voi
   const size_t o_err = take(4), o_step = take(2 * 4), o_gen = take(2 * 4), o_am = take(4);
   const size_t o_bw = take((size_t)grid * 16), o_kvf = take((size_t)c->n_layers * nkv * 4);
   const size_t o_pf = take(c->ffn_split ? (size_t)grid * H * 8 : 8);
+  const size_t o_bar = take(8);
   if ((st = cu(cudaMalloc(&x->scratch, off))) != TINFER_OK) return fail(st);
   if ((st = cu(cudaMemset(x->scratch, 0, off))) != TINFER_OK) return fail(st);
   uint8_t* s = (uint8_t*)x->scratch;
@@ -443,6 +444,9 @@ tinfer_status tinfer_create(const tinfer_config* c, const tinfer_weights* w, voi
   p.xa = (uint64_t*)(s + o_xa); p.xb = (uint64_t*)(s + o_xb); p.qkv = (uint64_t*)(s + o_qkv);
   p.attn = (uint64_t*)(s + o_attn); p.act = (uint64_t*)(s + o_act);
   p.part_ffn = (uint64_t*)(s + o_pf);
+  p.sync_barrier = 0;
+  p.bar_count = (unsigned long long*)(s + o_bar);
+  p.bar_base = 0;
   p.epoch = 1;  // the buffers start zeroed: stamp 0 is never expected
   p.stamp_check = c->exec_mode == TINFER_MEGAKERNEL;
   p.part_m = (float*)(s + o_pm); p.part_l = (float*)(s + o_pl); p.part_o = (float*)(s + o_po);
@@ -548,6 +552,7 @@ static tinfer_status step_impl(tinfer_ctx* x, int token, const int* token_dev, i
     TRY_CUDA(launch_megakernel(p, x->smem_mega, st));
     x->p.dbg_skip_cta = -1;  // an injected fault applies to one step only
     x->p.epoch += (unsigned)(x->cfg.n_layers * PHASES_PER_LAYER + 2);  // fresh stamps for the next step
+    if (x->p.sync_barrier) x->p.bar_base += (unsigned long long)(x->cfg.n_layers * PHASES_PER_LAYER);
     return TINFER_OK;
   }
   if (!x->gexec || x->graph_logits != logits || x->graph_argmax != argmax)
@@ -599,6 +604,7 @@ tinfer_status tinfer_generate_dev(tinfer_ctx* x, int32_t first_token, int32_t po
   TRY_CUDA(launch_megakernel(p, x->smem_mega, st));
   x->p.dbg_skip_cta = -1;
   x->p.epoch += (unsigned)n_steps * (unsigned)(x->cfg.n_layers * PHASES_PER_LAYER + 2);
+  if (x->p.sync_barrier) x->p.bar_base += (unsigned long long)n_steps * (unsigned long long)(x->cfg.n_layers * PHASES_PER_LAYER);
   return TINFER_OK;
 }
 
@@ -611,6 +617,8 @@ tinfer_status tinfer_get_error(tinfer_ctx* x) {
     uint8_t* s = (uint8_t*)x->scratch;
     TRY_CUDA(cudaMemset(s + x->err_off, 0, 4));
     TRY_CUDA(cudaMemset(s + x->tickets_off, 0, (size_t)(x->cfg.n_kv_heads + 1) * 4));
+    TRY_CUDA(cudaMemset(x->p.bar_count, 0, 8));
+    x->p.bar_base = 0;
     TRY_CUDA(cudaDeviceSynchronize());
     *reinterpret_cast<volatile int*>(x->err_host) = 0;
   }
@@ -680,6 +688,17 @@ tinfer_status tinfer_set_schedule(tinfer_ctx* x, int knob, long long value) {
       if (value < 0 || value > MAX_STAGES) return TINFER_ERR_INVALID_ARG;
       p.inflight_lm = (int)value;
       break;
+    case TINFER_S_SYNC:
+      if (value != TINFER_SYNC_STAMPS && value != TINFER_SYNC_GRID_BARRIER) return TINFER_ERR_INVALID_ARG;
+      if (x->cfg.exec_mode != TINFER_MEGAKERNEL) return TINFER_ERR_UNSUPPORTED;
+      if (value == TINFER_SYNC_GRID_BARRIER && !p.sync_barrier) {
+        // a fresh count: nothing of the context is running (the caller's stream order)
+        TRY_CUDA(cudaDeviceSynchronize());
+        TRY_CUDA(cudaMemset(p.bar_count, 0, 8));
+        p.bar_base = 0;
+      }
+      p.sync_barrier = (int)value;
+      break;
     default:
       return TINFER_ERR_INVALID_ARG;
   }
@@ -692,6 +711,7 @@ long long tinfer_get_schedule(const tinfer_ctx* x, int knob) {
   switch (knob) {
     case TINFER_S_L2_LOOKAHEAD: return x->p.l2_lookahead;
     case TINFER_S_L2_PACE: return x->p.l2_pace_ns_per_kb;
+    case TINFER_S_SYNC: return x->p.sync_barrier;
     case TINFER_S_INFLIGHT: return x->p.inflight;
     case TINFER_S_INFLIGHT_LM: return x->p.inflight_lm;
   }

@@ -90,6 +90,9 @@ struct __align__(16) StepParams {
   uint64_t* act;           // [F]
   uint64_t* part_ffn;      // [grid][H] column-split down projection: per-CTA partial sums (stamped)
   unsigned epoch;          // stamps of this launch: phase k writes epoch + k
+  int sync_barrier;        // 1: a grid barrier before every phase (the grid-barrier schedule)
+  unsigned long long* bar_count;  // its monotonic arrival counter
+  unsigned long long bar_base;    // barriers completed before this launch
   int stamp_check;         // readers wait for the stamp (persistent kernel); 0: stream order suffices
   float* part_m;           // [nq][nch_cap]      (per-phase kernels: ticket merge)
   float* part_l;           // [nq][nch_cap]

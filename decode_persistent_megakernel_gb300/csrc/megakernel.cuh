@@ -551,6 +551,30 @@ __device__ __forceinline__ bool run_phase(const StepParams& p, Pipe& pp, const G
   return run_gemv_phase<FMT, NCHL, IF, LOOP, SPLIT>(p, pp, pl, phase, tid, k, trace);
 }
 
+// The grid-barrier schedule ("Decoding in tiles", section 4: every wave ends at a grid barrier that
+// all workers pass): barrier number n of the context completes when the monotonic counter reaches
+// (n + 1) * grid. Thread 0 arrives with release semantics (ordering, through the consumer barrier
+// before it, the CTA's results of the previous phase) and waits with acquire semantics, bounded.
+__device__ __forceinline__ bool grid_barrier(const StepParams& p, Pipe& pp, unsigned long long n, int tid) {
+  named_sync(BAR_CONS, NCT);
+  if (tid == 0) {
+    red_add_release_u64(p.bar_count, 1ull);
+    const unsigned long long target = (n + 1ull) * (unsigned long long)p.grid;
+    if (ld_acquire_u64(p.bar_count) < target) {
+      const uint64_t t0 = globaltimer();
+      while (ld_acquire_u64(p.bar_count) < target) {
+        if (ld_volatile_int(p.err) != 0 || (long long)(globaltimer() - t0) > p.timeout_ns) {
+          if (ld_volatile_int(p.err) == 0) raise_error(p.err, p.err_host, EW_TIMEOUT);
+          pp.ms->abort = 1;
+          break;
+        }
+      }
+    }
+  }
+  named_sync(BAR_CONS, NCT);
+  return !*reinterpret_cast<volatile int*>(&pp.ms->abort);
+}
+
 // Start-of-step decision, identical in every CTA: skip when an earlier step left an error, or when
 // the token id is out of range (CTA 0 records that).
 __device__ __forceinline__ bool step_prologue(const StepParams& p, int& token, int pos, int* s_tok) {
@@ -621,6 +645,11 @@ __global__ void __launch_bounds__(NTHREADS_MEGA, 1) decode_megakernel(const __gr
       unsigned long long* tr = s == 0 ? trace : nullptr;  // the timeline records the first step
       bool ok = true;
       for (int k = 0; k < nph && ok; ++k) {
+        if (p.sync_barrier && k > 0 &&
+            !grid_barrier(p, pp, p.bar_base + (unsigned long long)s * (unsigned long long)(nph - 1) + (unsigned long long)(k - 1), tid)) {
+          ok = false;
+          break;
+        }
         if (unsigned long long* t = trace_at(tr, p, k, TR_START)) if (tid == 0) *t = globaltimer();
         const GemvPlan plan = plan_phase(p, pp, k, token, tid, &s_tab, ep);
         ok = run_phase<FMT, NCHL, 4, LOOP, SPLIT>(p, pp, plan, k, pos, tid, tr, ep);

@@ -209,7 +209,14 @@ tinfer_status tinfer_debug_withhold_results(tinfer_ctx* ctx, int cta, int phase)
  * [0, 64 MiB] (lookahead), [0, 100000] (pace) or [0, 8] (copies) return TINFER_ERR_INVALID_ARG.
  * Takes effect from the next step; results do not depend on it. tinfer_get_schedule returns the
  * current value, or -1 for an unknown knob. */
-enum { TINFER_S_INFLIGHT = 0, TINFER_S_INFLIGHT_LM = 1, TINFER_S_L2_LOOKAHEAD = 2, TINFER_S_L2_PACE = 3 };
+enum { TINFER_S_INFLIGHT = 0, TINFER_S_INFLIGHT_LM = 1, TINFER_S_L2_LOOKAHEAD = 2, TINFER_S_L2_PACE = 3,
+       TINFER_S_SYNC = 4 };
+/* TINFER_S_SYNC: how a phase waits for the one before it. TINFER_SYNC_STAMPS (default): each CTA
+ * waits only for the stamped results it reads. TINFER_SYNC_GRID_BARRIER: every CTA also passes a
+ * grid barrier before every phase ("Decoding in tiles", section 4: every wave ends at a grid
+ * barrier), for comparison. Persistent kernel only (TINFER_ERR_UNSUPPORTED in graph mode); switching
+ * to it synchronises the device. */
+enum { TINFER_SYNC_STAMPS = 0, TINFER_SYNC_GRID_BARRIER = 1 };
 tinfer_status tinfer_set_schedule(tinfer_ctx* ctx, int knob, long long value);
 long long tinfer_get_schedule(const tinfer_ctx* ctx, int knob);
 

@@ -198,3 +198,48 @@ def test_create_destroy_cycles():
         eng.step(1, 0)
         assert eng.error() == T.TINFER_OK
         eng.close()
+
+
+def test_grid_barrier_schedule_matches_oracle_and_stamped_schedule():
+    """The grid-barrier schedule (TINFER_SYNC_GRID_BARRIER) computes the same step as the stamped
+    hand-off: teacher-forced against the oracle, and bitwise equal to the default schedule."""
+    c = synth.config("tiny", max_ctx=300)
+    w = synth.make_model(c, seed=6)
+    outs = []
+    for sync in (T.TINFER_SYNC_GRID_BARRIER, T.TINFER_SYNC_STAMPS):
+        K, V = synth.make_kv(c, 270, seed=6)
+        eng = T.Engine(c, w, kv=(K, V))
+        assert T.tinfer_set_schedule(eng.ctx, T.TINFER_S_SYNC, sync) == 0
+        assert T.tinfer_get_schedule(eng.ctx, T.TINFER_S_SYNC) == sync
+        om = ORC.model(c, w)
+        toks = synth.make_tokens(c, 6, seed=6)
+        seq = []
+        for k, t in enumerate(toks.tolist()):
+            eng.step(t, 270 + k)
+            torch.cuda.synchronize()
+            got = eng.logits.cpu().numpy().copy()
+            ref, _, rc = ORC.decode_step(om, t, 270 + k, K, V)
+            err, rel, _ = compare_logits(got, ref)
+            assert err <= LOGIT_MAX_ABS and rel <= LOGIT_REL_L2, (sync, k, err, rel)
+            seq.append(got)
+        assert eng.error() == T.TINFER_OK
+        outs.append(np.stack(seq))
+        eng.close()
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+
+
+def test_grid_barrier_schedule_reports_a_withheld_result():
+    c = synth.config("tiny", max_ctx=8)
+    w = synth.make_model(c)
+    eng = T.Engine(c, w)
+    assert T.tinfer_set_schedule(eng.ctx, T.TINFER_S_SYNC, T.TINFER_SYNC_GRID_BARRIER) == 0
+    assert T.tinfer_set_timeout_ns(eng.ctx, 20_000_000) == 0
+    assert T.tinfer_debug_withhold_results(eng.ctx, 3, 2) == 0
+    eng.step(5, 0)
+    assert eng.error() == T.TINFER_ERR_TIMEOUT
+    eng.step(5, 0)  # the context recovers, counter included
+    assert eng.error() == T.TINFER_OK
+    eng.close()
+    eng = T.Engine(c, w, T.TINFER_GRAPH)
+    assert T.tinfer_set_schedule(eng.ctx, T.TINFER_S_SYNC, T.TINFER_SYNC_GRID_BARRIER) == T.TINFER_ERR_UNSUPPORTED
+    eng.close()
