@@ -95,6 +95,7 @@ class Oracle:
             "orc_swiglu": ([P, P, I, P], None),
             "orc_argmax": ([P, I, ctypes.POINTER(I)], I),
             "orc_decode_step": ([ctypes.POINTER(_Model), I, I, P, P, P, ctypes.POINTER(I), P], I),
+            "orc_moe_mlp": ([I, I, I, I, I, P, P, P, P, P, P, I, P, P, P, P], None),
         }
         for name, (args, res) in sig.items():
             f = getattr(lib, name)
@@ -196,6 +197,24 @@ class Oracle:
         a = np.empty_like(g)
         self.lib.orc_swiglu(_p(g), _p(u), g.size, _p(a))
         return a
+
+    def moe_mlp(self, fmt, group, scale_is_bf16, wg, sg, wu, su, wd, sd, ids, weights, x):
+        """Gathered-expert SwiGLU MLP (orc_moe_mlp): expert matrices stacked along the first axis,
+        wg, wu [E][ffn_e][...] and wd [E][hidden][...] (bf16 bits or int4 bytes, scales alike)."""
+        def c(a, t):
+            return None if a is None else np.ascontiguousarray(a, t)
+        wt = np.uint8 if fmt == 1 else np.uint16
+        wg, wu, wd = c(wg, wt), c(wu, wt), c(wd, wt)
+        sg, su, sd = c(sg, np.uint16), c(su, np.uint16), c(sd, np.uint16)
+        hidden = wd.shape[1]
+        ffn_e = wg.shape[1]
+        ids = np.ascontiguousarray(ids, np.int32)
+        weights = self._r(weights)
+        x = self._r(x)
+        y = np.empty(hidden, self.real)
+        self.lib.orc_moe_mlp(int(fmt), int(group), int(scale_is_bf16), hidden, ffn_e, _p(wg), _p(sg), _p(wu),
+                             _p(su), _p(wd), _p(sd), ids.size, _p(ids), _p(weights), _p(x), _p(y))
+        return y
 
     def argmax(self, logits):
         x = self._r(logits)

@@ -313,6 +313,42 @@ static void gemv_any(const orc_model* m, const void* w, const uint16_t* s, int r
  *   n_f = rmsnorm(x, g_final); logits = W_lm n_f; argmax.
  * ("Decoding in tiles", section 2, Figure 3; "One launch per token", "The oracle, then the
  * kernels"). The cache must hold slots [0, pos) already. */
+/* Gathered-expert SwiGLU MLP ("One launch per token", "The same trick, sparser: a 64-expert MoE"):
+ * for each chosen expert i in order, its gate and up projections of x, the SwiGLU of the two, its
+ * down projection of that, scaled by weight[i] and added to y. Weights stay in their stored format
+ * and are decoded exactly per row, as in the dense linears. */
+static void orc_linear(int fmt, int group, int scale_is_bf16, const void* w, const uint16_t* s,
+                       size_t expert, int rows, int cols, const orc_real* x, orc_real* y) {
+  if (fmt == ORC_INT4)
+    orc_gemv_int4((const uint8_t*)w + expert * (size_t)rows * (cols / 2),
+                  s + expert * (size_t)rows * (cols / group), scale_is_bf16, rows, cols, group, x, y);
+  else
+    orc_gemv_bf16((const uint16_t*)w + expert * (size_t)rows * cols, rows, cols, x, y);
+}
+
+void orc_moe_mlp(int weight_format, int group, int scale_is_bf16, int hidden, int ffn_e,
+                 const void* wg, const uint16_t* sg, const void* wu, const uint16_t* su,
+                 const void* wd, const uint16_t* sd, int top_k, const int32_t* ids,
+                 const orc_real* weights, const orc_real* x, orc_real* y) {
+  orc_real* g = (orc_real*)malloc(sizeof(orc_real) * (size_t)ffn_e);
+  orc_real* u = (orc_real*)malloc(sizeof(orc_real) * (size_t)ffn_e);
+  orc_real* a = (orc_real*)malloc(sizeof(orc_real) * (size_t)ffn_e);
+  orc_real* d = (orc_real*)malloc(sizeof(orc_real) * (size_t)hidden);
+  for (int o = 0; o < hidden; ++o) y[o] = 0;
+  for (int i = 0; i < top_k; ++i) {
+    const size_t e = (size_t)ids[i];
+    orc_linear(weight_format, group, scale_is_bf16, wg, sg, e, ffn_e, hidden, x, g);
+    orc_linear(weight_format, group, scale_is_bf16, wu, su, e, ffn_e, hidden, x, u);
+    orc_swiglu(g, u, ffn_e, a);
+    orc_linear(weight_format, group, scale_is_bf16, wd, sd, e, hidden, ffn_e, a, d);
+    for (int o = 0; o < hidden; ++o) y[o] += weights[i] * d[o];
+  }
+  free(g);
+  free(u);
+  free(a);
+  free(d);
+}
+
 int orc_decode_step(const orc_model* m, int token, int pos, uint16_t* kcache, uint16_t* vcache,
                     orc_real* logits, int* argmax, orc_real* trace_x) {
   const int H = m->hidden, nq = m->n_heads, nkv = m->n_kv_heads, d = m->head_dim;

@@ -82,6 +82,17 @@ void orc_attention_combine(const orc_real* m, const orc_real* l, const orc_real*
 void orc_swiglu(const orc_real* gate, const orc_real* up, int n, orc_real* a);
 int  orc_argmax(const orc_real* logits, int n, int* idx);
 
+/* Gathered-expert SwiGLU MLP ("One launch per token", section "The same trick, sparser: a 64-expert
+ * MoE": the router's chosen expert ids sit in a tensor, one kernel computes the gated/up SwiGLU of
+ * the chosen experts gathered by id, another the down projection and the weighted sum):
+ *   y = sum_{i < top_k} weight[i] * Wd[id_i] (silu(Wg[id_i] x) * (Wu[id_i] x)).
+ * Expert e's matrices: gate, up [ffn_e][hidden] and down [hidden][ffn_e], stored expert after expert
+ * (bf16 bits, or int4 bytes with scales as in the dense linears); x [hidden], y [hidden]. */
+void orc_moe_mlp(int weight_format, int group, int scale_is_bf16, int hidden, int ffn_e,
+                 const void* wg, const uint16_t* sg, const void* wu, const uint16_t* su,
+                 const void* wd, const uint16_t* sd, int top_k, const int32_t* ids,
+                 const orc_real* weights, const orc_real* x, orc_real* y);
+
 /* the whole step: embed, n_layers decoder layers, final norm, LM head, argmax. Writes K/V of
  * every layer at slot `pos` and attends over [0, pos]. trace_x (optional, [n_layers][hidden])
  * receives the residual stream after each layer. */

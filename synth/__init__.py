@@ -239,3 +239,33 @@ def model_bytes(cfg: dict) -> dict:
         per_layer += (cfg["n_heads"] + 2 * cfg["n_kv_heads"]) * cfg["head_dim"] * 2
     return dict(per_layer=per_layer, layers=per_layer * cfg["n_layers"], embed=V * H * 2,
                 lm_head=V * H * 2, final_norm=H * 2)
+
+
+def make_moe(n_experts: int, top_k: int, hidden: int, ffn_e: int, weight_format: str = "bf16",
+             group_size: int = 64, scale_dtype: str = "fp16", seed: int = 0) -> dict:
+    """One gathered-expert MLP case: every expert's gate and up [ffn_e][hidden] and down
+    [hidden][ffn_e] matrices stacked along the first axis (bf16 ~ N(0, 0.02), or int4 nibbles with
+    scales |N(0, 0.005)|), top_k distinct expert ids drawn uniformly from [0, n_experts), positive
+    routing weights (|N(0, 1)| normalised to sum 1, held as float32) and an input vector x ~ N(0, 1)
+    (float32)."""
+    m = {}
+    for name, rows, cols in (("g", ffn_e, hidden), ("u", ffn_e, hidden), ("d", hidden, ffn_e)):
+        key = f"moe.w{name}"
+        if weight_format == "int4":
+            m["w" + name] = nibbles(key, (n_experts, rows, cols // 2), seed)
+            m["s" + name] = abs_normal_16(key + ".scale", (n_experts, rows, cols // group_size), SCALE_STD,
+                                          scale_dtype, seed)
+        else:
+            m["w" + name] = normal_bf16(key, (n_experts, rows, cols), 0.0, WEIGHT_STD, seed)
+            m["s" + name] = None
+    # distinct ids: the first top_k of a seeded shuffle (Fisher-Yates on the generator's words)
+    order = list(range(n_experts))
+    r = words("moe.ids", n_experts, seed)
+    for i in range(n_experts - 1, 0, -1):
+        j = int(r[i] % np.uint64(i + 1))
+        order[i], order[j] = order[j], order[i]
+    m["ids"] = np.array(order[:top_k], dtype=np.int32)
+    w = np.abs(normals("moe.weights", top_k, seed))
+    m["weights"] = (w / w.sum()).astype(np.float32)
+    m["x"] = normals("moe.x", hidden, seed).astype(np.float32)
+    return m

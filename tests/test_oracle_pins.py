@@ -7,6 +7,7 @@ import numpy as np
 import pytest
 import torch
 
+import synth
 from oracle import Oracle, ERR_NONFINITE, ERR_INVALID
 
 ORC = Oracle("f64")
@@ -307,3 +308,67 @@ def test_oracle_f32_build_is_float():
     x = np.random.default_rng(15).standard_normal(100)
     W = bf16_bits(0.02 * np.random.default_rng(16).standard_normal((50, 100)))
     np.testing.assert_allclose(o32.gemv_bf16(W, x), ORC.gemv_bf16(W, x), rtol=1e-5, atol=1e-6)
+
+
+# ---------------------------------------------------------------- gathered-expert MLP
+
+def _moe(fmt="bf16", E=6, k=3, H=64, F=96, seed=0):
+    return synth.make_moe(E, k, H, F, fmt, 32, "bf16" if fmt == "int4" else "fp16", seed)
+
+
+def _dense_mlp(orc, m, e, fmt):
+    # the dense SwiGLU MLP of expert e from the pinned blocks
+    if fmt == "int4":
+        g = orc.gemv_int4(m["wg"][e], m["sg"][e], 1, 32, m["x"])
+        u = orc.gemv_int4(m["wu"][e], m["su"][e], 1, 32, m["x"])
+        return orc.gemv_int4(m["wd"][e], m["sd"][e], 1, 32, orc.swiglu(g, u))
+    g = orc.gemv_bf16(m["wg"][e], m["x"])
+    u = orc.gemv_bf16(m["wu"][e], m["x"])
+    return orc.gemv_bf16(m["wd"][e], orc.swiglu(g, u))
+
+
+def _moe_call(orc, m, fmt, ids, weights):
+    f = 1 if fmt == "int4" else 0
+    return orc.moe_mlp(f, 32, 1, m["wg"], m["sg"], m["wu"], m["su"], m["wd"], m["sd"], ids, weights, m["x"])
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "int4"])
+def test_moe_one_expert_is_the_dense_mlp(fmt):
+    # top-1 with weight 1 reduces to the dense SwiGLU MLP of that expert, gathered by its id
+    m = _moe(fmt)
+    for e in (0, 4):
+        got = _moe_call(ORC, m, fmt, [e], [1.0])
+        assert np.array_equal(got, _dense_mlp(ORC, m, e, fmt))
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "int4"])
+def test_moe_is_the_weighted_sum_of_the_chosen_experts(fmt):
+    m = _moe(fmt, seed=1)
+    ids, w = m["ids"], m["weights"].astype(np.float64)
+    got = _moe_call(ORC, m, fmt, ids, w)
+    want = sum(wi * _dense_mlp(ORC, m, int(e), fmt) for e, wi in zip(ids, w))
+    assert np.allclose(got, want, rtol=1e-13, atol=1e-15)
+    # each expert is read at its own id: a gather from the wrong slot fails this
+    assert not np.allclose(got, sum(wi * _dense_mlp(ORC, m, (int(e) + 1) % 6, fmt) for e, wi in zip(ids, w)))
+
+
+def test_moe_routing_invariants():
+    m = _moe(seed=2)
+    ids, w = m["ids"], m["weights"].astype(np.float64)
+    base = _moe_call(ORC, m, "bf16", ids, w)
+    # the order of the chosen experts does not matter
+    perm = np.array([2, 0, 1])
+    assert np.allclose(_moe_call(ORC, m, "bf16", ids[perm], w[perm]), base, rtol=1e-13, atol=1e-15)
+    # an expert chosen with weight 0 adds nothing (exactly)
+    got = _moe_call(ORC, m, "bf16", np.append(ids, 5), np.append(w, 0.0))
+    assert np.array_equal(got, base)
+    # linear in the routing weights: one id twice counts as once with the summed weight
+    two = _moe_call(ORC, m, "bf16", [ids[0], ids[0]], [0.25, 0.5])
+    assert np.allclose(two, _moe_call(ORC, m, "bf16", [ids[0]], [0.75]), rtol=1e-13, atol=1e-15)
+
+
+def test_moe_synthetic_case_is_valid():
+    m = synth.make_moe(64, 8, 2048, 1024)
+    assert len(set(m["ids"].tolist())) == 8 and m["ids"].min() >= 0 and m["ids"].max() < 64
+    assert abs(float(m["weights"].sum()) - 1.0) < 1e-6 and (m["weights"] > 0).all()
+    assert m["wg"].shape == (64, 1024, 2048) and m["wd"].shape == (64, 2048, 1024)
