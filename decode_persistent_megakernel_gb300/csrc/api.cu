@@ -880,6 +880,86 @@ tinfer_status tinfer_op_attention(int nq, int nkv, int d, int max_ctx, double th
   return rc;
 }
 
+size_t tinfer_moe_packed_bytes(int fmt, int group, int n_experts, int hidden, int ffn_e, int which) {
+  if (n_experts <= 0) return 0;
+  const size_t rbh = packed_row_bytes(fmt, hidden, group), rbf = packed_row_bytes(fmt, ffn_e, group);
+  if (!rbh || !rbf) return 0;
+  return which == 0 ? (size_t)n_experts * 2 * ffn_e * rbh : (size_t)n_experts * hidden * rbf;
+}
+
+tinfer_status tinfer_pack_moe(int fmt, int group, int scale_dtype, int n_experts, int hidden, int ffn_e,
+                              const void* wg, const void* sg, const void* wu, const void* su,
+                              const void* wd, const void* sd, void* gu_packed_dev, void* down_packed_dev,
+                              void* stream) {
+  (void)scale_dtype;
+  if (!tinfer_moe_packed_bytes(fmt, group, n_experts, hidden, ffn_e, 0) || !gu_packed_dev || !down_packed_dev)
+    return TINFER_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(gu_packed_dev) & 15) || (reinterpret_cast<uintptr_t>(down_packed_dev) & 15))
+    return TINFER_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  // every expert's gate rows land on even packed rows and its up rows on odd ones: expert e's row j
+  // is stacked row e * ffn_e + j, packed row 2 (e * ffn_e + j) (+ 1)
+  TRY(pack_one(fmt, group, wg, sg, n_experts * ffn_e, hidden, (uint8_t*)gu_packed_dev, 2, 0, st));
+  TRY(pack_one(fmt, group, wu, su, n_experts * ffn_e, hidden, (uint8_t*)gu_packed_dev, 2, 1, st));
+  TRY(pack_one(fmt, group, wd, sd, n_experts * hidden, ffn_e, (uint8_t*)down_packed_dev, 1, 0, st));
+  return TINFER_OK;
+}
+
+tinfer_status tinfer_op_moe(int fmt, int group, int scale_dtype, int n_experts, int top_k, int hidden,
+                            int ffn_e, const void* gu_packed_dev, const void* down_packed_dev,
+                            const int32_t* ids_dev, const float* weights_dev, const float* x_dev,
+                            float* h_dev, float* y_dev, int accumulate, int32_t* status_dev,
+                            void* stream) {
+  if (!tinfer_moe_packed_bytes(fmt, group, n_experts, hidden, ffn_e, 0)) return TINFER_ERR_INVALID_ARG;
+  if (top_k < 1 || top_k > n_experts || NCW % top_k != 0) return TINFER_ERR_UNSUPPORTED;
+  if (!gu_packed_dev || !down_packed_dev || !ids_dev || !weights_dev || !x_dev || !h_dev || !y_dev)
+    return TINFER_ERR_INVALID_ARG;
+  for (const void* ptr : {gu_packed_dev, down_packed_dev, (const void*)x_dev, (const void*)h_dev, (const void*)y_dev})
+    if (reinterpret_cast<uintptr_t>(ptr) & 15) return TINFER_ERR_INVALID_ARG;
+  if (accumulate != 0 && accumulate != 1) return TINFER_ERR_INVALID_ARG;
+  // the gate/up GEMV reads rows of `hidden` inputs; the down projection gives each expert one warp
+  // group and a segment of ffn_e inputs, whose activations a lane keeps in registers
+  const int E = fmt == TINFER_INT4 ? 32 : 8;
+  if (!seg_ok(fmt, hidden) || ffn_e % E || ffn_e / E > 32 * (fmt == TINFER_INT4 ? 2 : 8))
+    return TINFER_ERR_UNSUPPORTED;
+  int nchl = 4;
+  if (fmt == TINFER_BF16) {
+    const int need = std::max((seg_info(0, hidden).chs + 31) / 32, (ffn_e / 8 + 31) / 32);
+    nchl = need <= 4 ? 4 : 8;
+  }
+  int dev = 0, sms = 0;
+  TRY_CUDA(cudaGetDevice(&dev));
+  TRY_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  TRY(op_scratch());
+  OpMoeParams q{};
+  q.gu = (const uint8_t*)gu_packed_dev; q.down = (const uint8_t*)down_packed_dev;
+  q.ids = ids_dev; q.weights = weights_dev; q.x = x_dev; q.h = h_dev; q.y = y_dev; q.status = status_dev;
+  q.n_experts = n_experts; q.k = top_k; q.hidden = hidden; q.ffn_e = ffn_e;
+  q.rb_h = (int)packed_row_bytes(fmt, hidden, group); q.rb_f = (int)packed_row_bytes(fmt, ffn_e, group);
+  q.fmt = fmt; q.group = group; q.scale_bf16 = scale_dtype == TINFER_SCALE_BF16; q.nchl = nchl;
+  q.accumulate = accumulate; q.err = g_op.err; q.timeout_ns = DEFAULT_TIMEOUT_NS;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (status_dev) TRY_CUDA(cudaMemsetAsync(status_dev, 0, 4, st));
+  // rows of one CTA's share must fit the shared row-result buffer
+  const long long rows_a = ((long long)top_k * 2 * ffn_e + sms - 1) / sms + 2, rows_b = (hidden + sms - 1) / sms + 1;
+  if (rows_a * seg_info(fmt, hidden).nseg > ROWV_MAX || rows_b * top_k > ROWV_MAX) return TINFER_ERR_UNSUPPORTED;
+  // gate/up: 4 stages of 32 KB (several rows of `hidden` inputs each)
+  q.stages = 4;
+  q.slot = (int)std::max<size_t>(SLOT_MIN, align_up((size_t)q.rb_h * 2, 1024));
+  size_t smem = smem_for(q.stages, q.slot, (int)align_up((size_t)hidden * 4, 128));
+  if (smem > 227 * 1024) return TINFER_ERR_UNSUPPORTED;
+  TRY_CUDA(set_smem_op_moe(fmt, nchl, 0, smem));
+  TRY_CUDA(launch_op_moe(q, 0, sms, smem, st));
+  // down: 3 stages, each holding a few rows of every chosen expert
+  q.stages = 3;
+  q.slot = (int)std::max<size_t>(48 * 1024, align_up((size_t)top_k * q.rb_f * (NCW / top_k), 1024));
+  smem = smem_for(q.stages, q.slot, (int)align_up((size_t)top_k * ffn_e * 4, 128));
+  if (smem > 227 * 1024) return TINFER_ERR_UNSUPPORTED;
+  TRY_CUDA(set_smem_op_moe(fmt, nchl, 1, smem));
+  TRY_CUDA(launch_op_moe(q, 1, sms, smem, st));
+  return TINFER_OK;
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------------- attention without allocation

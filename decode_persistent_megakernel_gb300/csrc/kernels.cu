@@ -92,6 +92,137 @@ __global__ void __launch_bounds__(NTHREADS, 1) op_attention_kernel(const __grid_
   __syncthreads();
 }
 
+// ------------------------------------------------------------------------------ gathered experts
+
+// The chosen expert ids in shared memory; an id outside [0, n_experts) reads expert 0 and is
+// reported through q.status (the kernels never address outside the packed experts).
+__device__ __forceinline__ void moe_load_ids(const OpMoeParams& q, int* s_ids) {
+  if (threadIdx.x < (unsigned)q.k) {
+    int e = q.ids[threadIdx.x];
+    if (e < 0 || e >= q.n_experts) {
+      if (q.status) atomicExch(q.status, 1);
+      e = 0;
+    }
+    s_ids[threadIdx.x] = e;
+  }
+}
+
+// Gate/up of the chosen experts ("One launch per token", "The same trick, sparser: a 64-expert MoE":
+// one kernel does the gated/up SwiGLU for the selected experts gathered by id). The matrix is the k
+// experts' interleaved gate/up rows one after another, k * 2 ffn_e "virtual" rows; the producer
+// gathers each stage from the experts its rows belong to (two bulk copies when a stage straddles
+// two experts), and the consumers run the ordinary GEMV with the SwiGLU epilogue into h [k][ffn_e].
+template <int FMT, int NCHL>
+__global__ void __launch_bounds__(NTHREADS, 1) op_moe_gu_kernel(const __grid_constant__ OpMoeParams q) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ int s_ids[G_MAX];
+  Pipe pp;
+  pipe_init(pp, smem, q.stages, q.slot, q.timeout_ns, q.err, nullptr);
+  pipe_setup(pp);
+  moe_load_ids(q, s_ids);
+  __syncthreads();
+  const int per = 2 * q.ffn_e;  // virtual rows per expert
+  const GemvDesc g{nullptr, q.k * per, q.hidden, q.rb_h, q.fmt, q.group, q.scale_bf16, 2};
+  const RowSplit rs = row_split(g, blockIdx.x, gridDim.x, q.slot);
+  const int tid = threadIdx.x;
+  if (tid >= NCT) {
+    if (tid == NCT) {
+      bool dead = false;
+      const uint64_t pol = policy_evict_first();
+      for (int s0 = rs.r0; s0 < rs.r1 && !dead; s0 += rs.nr) {
+        const int nrs = min(rs.nr, rs.r1 - s0);
+        uint32_t dst, bar;
+        if (!prod_open(pp, (uint32_t)(nrs * q.rb_h), dst, bar, dead)) break;
+        for (int v = s0; v < s0 + nrs;) {
+          const int i = v / per, r = v - i * per, n = min(s0 + nrs - v, per - r);
+          const uint8_t* src = q.gu + ((size_t)s_ids[i] * per + r) * q.rb_h;
+          bulk_g2s(dst + (uint32_t)(v - s0) * q.rb_h, src, (uint32_t)(n * q.rb_h), bar, pol);
+          v += n;
+        }
+        pipe_advance(pp);
+      }
+      prod_drain(pp);
+    }
+  } else {
+    GemvPlan pl;
+    pl.g = g;
+    pl.rs = rs;
+    pl.src = ActSrc{};
+    pl.src.xf = q.x;
+    pl.src.n = q.hidden;
+    pl.epi = Epi{EK_SWIGLU, q.h, nullptr, nullptr, 0u, 0};
+    Best best{-CUDART_INF_F, 0x7FFFFFFF, 0};
+    if (FMT == 1) gemv_rows<1, 2>(pp, pl, best, tid, nullptr);
+    else gemv_rows<0, NCHL>(pp, pl, best, tid, nullptr);
+    if (tid == 0) *reinterpret_cast<volatile int*>(&pp.ms->cons_done) = 1;
+  }
+  __syncthreads();
+}
+
+// Down projections of the chosen experts and their weighted sum (the page's second kernel). Row o
+// of the gathered matrix is the concatenation of the k experts' row o; a stage holds its rows
+// expert after expert (segment-major: one bulk copy per expert), warp w takes expert w's segment
+// with its SwiGLU outputs h[w] in registers, and the epilogue adds the k segment sums weighted by
+// the routing weights, in order.
+template <int FMT, int NCHL>
+__global__ void __launch_bounds__(NTHREADS, 1) op_moe_down_kernel(const __grid_constant__ OpMoeParams q) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ int s_ids[G_MAX];
+  Pipe pp;
+  pipe_init(pp, smem, q.stages, q.slot, q.timeout_ns, q.err, nullptr);
+  pipe_setup(pp);
+  moe_load_ids(q, s_ids);
+  __syncthreads();
+  GemvDesc g{nullptr, q.hidden, q.k * q.ffn_e, q.k * q.rb_f, q.fmt, q.group, q.scale_bf16, 1};
+  g.nsegs = q.k;
+  g.rbs = q.rb_f;
+  RowSplit rs = row_split(g, blockIdx.x, gridDim.x, q.slot);
+  const int wg = NCW / q.k;
+  int fit = q.slot / (q.k * q.rb_f);
+  if (fit > NR_MAX) fit = NR_MAX;
+  rs.nr = fit - fit % wg;
+  const int tid = threadIdx.x;
+  if (tid >= NCT) {
+    if (tid == NCT) {
+      bool dead = false;
+      const uint64_t pol = policy_evict_first();
+      for (int s0 = rs.r0; s0 < rs.r1 && !dead; s0 += rs.nr) {
+        const int nrs = min(rs.nr, rs.r1 - s0);
+        const uint32_t seg_bytes = (uint32_t)(nrs * q.rb_f);
+        uint32_t dst, bar;
+        if (!prod_open(pp, seg_bytes * (uint32_t)q.k, dst, bar, dead)) break;
+        for (int i = 0; i < q.k; ++i)
+          bulk_g2s(dst + (uint32_t)i * seg_bytes, q.down + ((size_t)s_ids[i] * q.hidden + s0) * q.rb_f,
+                   seg_bytes, bar, pol);
+        pipe_advance(pp);
+      }
+      prod_drain(pp);
+    }
+  } else {
+    GemvPlan pl;
+    pl.g = g;
+    pl.rs = rs;
+    pl.src = ActSrc{};
+    pl.src.xf = q.h;
+    pl.src.n = q.k * q.ffn_e;
+    pl.epi = Epi{q.accumulate ? EK_RESIDUAL : EK_STORE, q.y, q.weights, nullptr, 0u, 0};
+    Best best{-CUDART_INF_F, 0x7FFFFFFF, 0};
+    if (FMT == 1) gemv_rows<1, 2, 4, true>(pp, pl, best, tid, nullptr);
+    else gemv_rows<0, NCHL, 4, true>(pp, pl, best, tid, nullptr);
+    if (tid == 0) *reinterpret_cast<volatile int*>(&pp.ms->cons_done) = 1;
+  }
+  __syncthreads();
+}
+
+static const void* moe_fn(int fmt, int nchl, int phase) {
+  if (fmt == 1) return phase ? (const void*)op_moe_down_kernel<1, 2> : (const void*)op_moe_gu_kernel<1, 2>;
+  switch (nchl) {
+    case 4: return phase ? (const void*)op_moe_down_kernel<0, 4> : (const void*)op_moe_gu_kernel<0, 4>;
+    case 8: return phase ? (const void*)op_moe_down_kernel<0, 8> : (const void*)op_moe_gu_kernel<0, 8>;
+  }
+  return nullptr;
+}
+
 // ------------------------------------------------------------------------------ packing
 
 // dst row (r * dst_step + dst_first) of width dst_rb <- src row r: src_bytes bytes of w, then
@@ -238,6 +369,13 @@ cudaError_t set_smem_mega(size_t b, int fmt, int nchl) {
 }
 cudaError_t set_smem_phase(size_t b, int fmt, int nchl) { return raise_limit(step_fn(fmt, nchl, 2), b); }
 cudaError_t set_smem_op_gemv(size_t b) { return raise_limit((const void*)op_gemv_kernel, b); }
+cudaError_t set_smem_op_moe(int fmt, int nchl, int phase, size_t b) { return raise_limit(moe_fn(fmt, nchl, phase), b); }
+cudaError_t launch_op_moe(const OpMoeParams& q, int phase, int grid, size_t smem, cudaStream_t st) {
+  const void* fn = moe_fn(q.fmt, q.nchl, phase);
+  if (!fn) return cudaErrorInvalidDeviceFunction;
+  void* args[] = {const_cast<OpMoeParams*>(&q)};
+  return cudaLaunchKernel(fn, dim3(grid), dim3(NTHREADS), args, smem, st);
+}
 cudaError_t set_smem_op_attention(size_t b) { return raise_limit((const void*)op_attention_kernel, b); }
 
 cudaError_t megakernel_occupancy(int* blocks_per_sm, size_t smem, int fmt, int nchl) {

@@ -44,6 +44,27 @@ struct OpAttnParams {
   long long timeout_ns;
 };
 
+// The gathered-expert MLP (two kernels: gate/up with SwiGLU over the chosen experts' rows, then the
+// down projections with the weighted sum).
+struct OpMoeParams {
+  const uint8_t* gu;      // packed gate/up rows of every expert, [n_experts][2 ffn_e] rows of rb_h bytes
+  const uint8_t* down;    // packed down rows of every expert, [n_experts][hidden] rows of rb_f bytes
+  const int* ids;         // [k] chosen experts
+  const float* weights;   // [k] their routing weights
+  const float* x;         // [hidden]
+  float* h;               // [k][ffn_e] SwiGLU outputs of the chosen experts
+  float* y;               // [hidden]
+  int* status;            // may be null: set to 1 when an id was outside [0, n_experts)
+  int n_experts, k, hidden, ffn_e, rb_h, rb_f;
+  int fmt, group, scale_bf16, nchl;
+  int accumulate;         // 0: y = MLP(x); 1: y += MLP(x)
+  int* err;
+  int stages, slot;
+  long long timeout_ns;
+};
+cudaError_t launch_op_moe(const OpMoeParams& q, int phase, int grid, size_t smem, cudaStream_t st);
+cudaError_t set_smem_op_moe(int fmt, int nchl, int phase, size_t bytes);
+
 cudaError_t launch_megakernel(const StepParams& p, size_t smem, cudaStream_t st);
 cudaError_t launch_phase(const StepParams& p, int k, size_t smem, cudaStream_t st, bool pdl);
 cudaError_t launch_begin(int* step_dev, int token, const int* token_dev, int pos, int V, int* err,

@@ -153,6 +153,33 @@ __device__ __forceinline__ void prod_push(Pipe& pp, const void* src, uint32_t by
   pipe_advance(pp);
 }
 
+// Producer: opens the next stage for `bytes` bytes, which the caller then fills with one or more
+// bulk copies into the shared address *dst completing on *bar, and closes with pipe_advance. False
+// (and dead set) when the consumers are gone or a wait ran out.
+__device__ __forceinline__ bool prod_open(Pipe& pp, uint32_t bytes, uint32_t& dst, uint32_t& bar, bool& dead) {
+  if (dead) return false;
+  const int s = pp.s;
+  if (!wait_bar(pp.empty0 + 8u * s, pp.ph ^ 1u, pp.timeout, &pp.ms->cons_done)) {
+    dead = true;
+    if (!*reinterpret_cast<volatile int*>(&pp.ms->cons_done)) raise_error(pp.err, pp.err_host, EW_TIMEOUT);
+    return false;
+  }
+  const int k = pp.inflight < pp.stages ? pp.inflight : pp.stages;
+  if (k > 0 && pp.it >= (uint32_t)k) {
+    const int s2 = s >= k ? s - k : s - k + pp.stages;
+    const uint32_t p2 = s >= k ? pp.ph : pp.ph ^ 1u;
+    if (!mbar_try_wait(pp.full0 + 8u * s2, p2) &&
+        !wait_bar(pp.full0 + 8u * s2, p2, pp.timeout, &pp.ms->cons_done)) {
+      dead = true;
+      return false;
+    }
+  }
+  bar = pp.full0 + 8u * s;
+  dst = pp.ring + (uint32_t)s * pp.slot;
+  mbar_arrive_expect_tx(bar, bytes);
+  return true;
+}
+
 // Before the CTA exits: every copy this producer issued has landed (bounded wait).
 static __device__ void prod_drain(Pipe& pp) {
   const uint32_t n = pp.it < (uint32_t)pp.stages ? pp.it : (uint32_t)pp.stages;
@@ -370,6 +397,9 @@ struct GemvDesc {
   int rows, cols, rb;
   int fmt, group, scale_bf16;
   int quantum;  // 2: rows come in (gate, up) pairs that one stage never splits
+  // segment-major stages (gemv_rows<..., SEGMAJOR>): a stage holds nsegs blocks, block s the stage's
+  // rows of segment s (rbs bytes per row), as gathered from nsegs separate matrices
+  int nsegs = 0, rbs = 0;
 };
 
 // Rows of a matrix owned by one CTA: an even split of row quanta; nr rows per ring stage.
@@ -590,7 +620,10 @@ struct GemvPlan {
 // segments in a fixed order and applies the epilogue (bias, residual add, SwiGLU on gate/up pairs).
 // IF: input blocks in flight per thread while fetching the input vector (four: eight made the
 // Llama-shaped bf16 step 8 % slower and the int4 instances spill).
-template <int FMT, int NCHL, int IF = 4>
+// SEGMAJOR: segment-major stages (GemvDesc::nsegs blocks of GemvDesc::rbs-byte rows), one warp group
+// per segment, and an epilogue that weighs the segment sums with epi.bias[s] before adding them in
+// order (the gathered-expert down projection: segment s is expert s's row).
+template <int FMT, int NCHL, int IF = 4, bool SEGMAJOR = false>
 __device__ __forceinline__ bool gemv_rows(Pipe& pp, const GemvPlan& pl, Best& best, int tid,
                           unsigned long long* tr_ready) {
   constexpr int E = FMT == 0 ? 8 : 32;
@@ -600,8 +633,7 @@ __device__ __forceinline__ bool gemv_rows(Pipe& pp, const GemvPlan& pl, Best& be
   const Epi& epi = pl.epi;
   Misc* ms = pp.ms;
   const int lane = tid & 31, warp = tid >> 5;
-  const SegInfo si = seg_info(FMT, g.cols);
-  const int nchl = (si.chs + 31) / 32;  // chunks per lane that hold inputs (<= NCHL)
+  const SegInfo si = SEGMAJOR ? SegInfo{g.nsegs, g.cols / g.nsegs, g.cols / g.nsegs / E} : seg_info(FMT, g.cols);
   const int seg = warp % si.nseg, grp = warp / si.nseg, WG = NCW / si.nseg;
   const int nrows = rs.r1 - rs.r0;
   const bool direct = epi.kind == EK_ARGMAX && si.nseg == 1;  // the warp holds whole rows
@@ -610,7 +642,7 @@ __device__ __forceinline__ bool gemv_rows(Pipe& pp, const GemvPlan& pl, Best& be
   float pre = 0.f;
   if (!direct && tid < nrows && epi.kind != EK_ARGMAX) {
     if (epi.kind == EK_RESIDUAL) pre = residual_at(epi, rs.r0 + tid);
-    else if (epi.kind == EK_STORE && epi.bias) pre = __ldg(epi.bias + rs.r0 + tid);
+    else if (epi.kind == EK_STORE && epi.bias && !SEGMAJOR) pre = __ldg(epi.bias + rs.r0 + tid);
   }
 
   // the input vector (x * g for RMSNorm phases) into shared memory, then this warp's segment into
@@ -656,16 +688,16 @@ __device__ __forceinline__ bool gemv_rows(Pipe& pp, const GemvPlan& pl, Best& be
   }
   if (tr_ready && tid == 0) *tr_ready = globaltimer();
 
-  const uint32_t seg_off = FMT == 0 ? (uint32_t)(seg * si.ks * 2) : (uint32_t)(seg * si.ks / 2);
+  const uint32_t seg_off = SEGMAJOR ? 0u : FMT == 0 ? (uint32_t)(seg * si.ks * 2) : (uint32_t)(seg * si.ks / 2);
   const uint32_t mag = opaque_u32(0x4B000000u);  // int4 exponent-trick magic, kept in a register
-  const uint32_t scale_off = (uint32_t)(g.cols / 2);
+  const uint32_t scale_off = (uint32_t)((SEGMAJOR ? si.ks : g.cols) / 2);
   // byte offsets inside a row of this lane's chunks (chunk k = lane + 32 k, clamped) and scales
   uint32_t coff[NCHL], soff[NCHL];
 #pragma unroll
   for (int k = 0; k < NCHL; ++k) {
     const int c = min(lane + 32 * k, si.chs - 1);
     coff[k] = seg_off + (uint32_t)c * 16u;
-    soff[k] = FMT == 1 ? scale_off + 2u * (uint32_t)((seg * si.ks + c * 32) / g.group) : 0u;
+    soff[k] = FMT == 1 ? scale_off + 2u * (uint32_t)(((SEGMAJOR ? 0 : seg * si.ks) + c * 32) / g.group) : 0u;
   }
 
   // The warp walks its rows stage by stage (rows grp, grp + WG, ... of each stage). Lane partials
@@ -701,7 +733,7 @@ __device__ __forceinline__ bool gemv_rows(Pipe& pp, const GemvPlan& pl, Best& be
     int i0 = grp;
 #pragma unroll 1
     for (int i = i0; i < nrs; i += WG) {
-      const uint32_t rowp = st + (uint32_t)i * g.rb;
+      const uint32_t rowp = SEGMAJOR ? st + (uint32_t)(seg * nrs + i) * (uint32_t)g.rbs : st + (uint32_t)i * g.rb;
       float2 acc = make_float2(0.f, 0.f), acc2 = make_float2(0.f, 0.f);
       // every chunk is loaded unconditionally (clamped offsets, zero activations past the row), so
       // that all loads of the row issue back to back
@@ -742,7 +774,11 @@ __device__ __forceinline__ bool gemv_rows(Pipe& pp, const GemvPlan& pl, Best& be
   } else {
     for (int t = tid; t < nrows; t += NCT) {
       float v = 0.f;
-      for (int s2 = 0; s2 < si.nseg; ++s2) v += ms->rowv[t * si.nseg + s2];
+      if (SEGMAJOR) {
+        for (int s2 = 0; s2 < si.nseg; ++s2) v = fmaf(__ldg(epi.bias + s2), ms->rowv[t * si.nseg + s2], v);
+      } else {
+        for (int s2 = 0; s2 < si.nseg; ++s2) v += ms->rowv[t * si.nseg + s2];
+      }
       const int r = rs.r0 + t;
       if (epi.kind == EK_ARGMAX) {
         if (epi.out) static_cast<float*>(epi.out)[r] = v;
@@ -750,8 +786,9 @@ __device__ __forceinline__ bool gemv_rows(Pipe& pp, const GemvPlan& pl, Best& be
         continue;
       }
       float base = pre;
-      if (t >= NCT) base = epi.kind == EK_RESIDUAL ? residual_at(epi, r) : (epi.bias ? epi.bias[r] : 0.f);
-      epi_write(epi, r, (epi.kind == EK_RESIDUAL || epi.bias) ? base + v : v);
+      const bool row_bias = epi.bias && !SEGMAJOR;  // segment-major: bias holds the segment weights
+      if (t >= NCT) base = epi.kind == EK_RESIDUAL ? residual_at(epi, r) : (row_bias ? epi.bias[r] : 0.f);
+      epi_write(epi, r, (epi.kind == EK_RESIDUAL || row_bias) ? base + v : v);
     }
   }
   return true;

@@ -262,6 +262,35 @@ tinfer_status tinfer_op_attention(int n_heads, int n_kv_heads, int head_dim, int
                                   float* part_m_dev, float* part_l_dev, float* part_o_dev,
                                   void* stream);
 
+/* Gathered-expert SwiGLU MLP of a mixture-of-experts layer ("One launch per token", section "The
+ * same trick, sparser: a 64-expert MoE": the router writes the chosen expert ids into a device
+ * tensor and two fixed-shape kernels read the weights through that index, one for the gated/up
+ * SwiGLU of the chosen experts, one for the down projection and the weighted sum):
+ *   y = sum_{i < top_k} weights[i] * Wd[ids[i]] (silu(Wg[ids[i]] x) * (Wu[ids[i]] x))   (accumulate 0)
+ *   y += the same                                                                       (accumulate 1)
+ * Canonical expert weights (device, stacked expert after expert): wg, wu [n_experts][ffn_e][hidden],
+ * wd [n_experts][hidden][ffn_e], bf16 or int4 with scales as in tinfer_layer_src. tinfer_pack_moe
+ * packs them into gu_packed (tinfer_moe_packed_bytes(..., 0) bytes: each expert's gate/up rows
+ * interleaved) and down_packed (..., 1); both 16-byte aligned, caller-owned. tinfer_op_moe: ids_dev
+ * (int32 [top_k]) and weights_dev (fp32 [top_k]) are read on the device when the kernels run, so the
+ * call has a fixed shape; x_dev (fp32 [hidden]), h_dev (fp32 [top_k][ffn_e], scratch that receives
+ * the SwiGLU outputs) and y_dev (fp32 [hidden]) are 16-byte aligned. An id outside [0, n_experts)
+ * reads expert 0 instead and sets *status_dev (int32, may be NULL; cleared first) to 1.
+ * Asynchronous on `stream`. Supported: top_k in {1, 2, 4, 8}, hidden a width the step supports,
+ * ffn_e a multiple of 8 (bf16) or 32 (int4) up to 2048; else TINFER_ERR_UNSUPPORTED. */
+size_t tinfer_moe_packed_bytes(int weight_format, int group_size, int n_experts, int hidden, int ffn_e,
+                               int which);
+tinfer_status tinfer_pack_moe(int weight_format, int group_size, int scale_dtype, int n_experts,
+                              int hidden, int ffn_e, const void* wg_dev, const void* sg_dev,
+                              const void* wu_dev, const void* su_dev, const void* wd_dev,
+                              const void* sd_dev, void* gu_packed_dev, void* down_packed_dev,
+                              void* stream);
+tinfer_status tinfer_op_moe(int weight_format, int group_size, int scale_dtype, int n_experts,
+                            int top_k, int hidden, int ffn_e, const void* gu_packed_dev,
+                            const void* down_packed_dev, const int32_t* ids_dev,
+                            const float* weights_dev, const float* x_dev, float* h_dev, float* y_dev,
+                            int accumulate, int32_t* status_dev, void* stream);
+
 /* ---------------------------------------------------------------------------------------------
  * Attention that allocates nothing. The pages have no counterpart of this call: it is an
  * engineering addition for embedders.
