@@ -31,7 +31,7 @@ EXPORTS = [
     "tinfer_generate", "tinfer_generate_dev", "tinfer_get_error", "tinfer_query", "tinfer_set_trace", "tinfer_set_timeout_ns",
     "tinfer_debug_withhold_results", "tinfer_set_schedule", "tinfer_get_schedule", "tinfer_destroy",
     "tinfer_packed_row_bytes", "tinfer_pack_matrix", "tinfer_op_gemv", "tinfer_op_attention",
-    "tinfer_op_attention_noalloc", "tinfer_moe_packed_bytes", "tinfer_pack_moe", "tinfer_op_moe",
+    "tinfer_op_attention_noalloc", "tinfer_op_gemv_batch", "tinfer_moe_packed_bytes", "tinfer_pack_moe", "tinfer_op_moe",
 ]
 
 
@@ -101,6 +101,7 @@ def lib():
             "tinfer_op_gemv": ([I, I, I, I, I, P, P, P, D, P, I, P, P, P], I),
             "tinfer_op_attention": ([I, I, I, I, D, I, I, P, P, P, P, P, P, P, P], I),
             "tinfer_op_attention_noalloc": ([I, I, I, I, D, I, I, P, P, P, P, P], I),
+            "tinfer_op_gemv_batch": ([I, I, I, I, I, I, P, P, P, I, P, P], I),
             "tinfer_moe_packed_bytes": ([I, I, I, I, I, I], Z),
             "tinfer_pack_moe": ([I, I, I, I, I, I, P, P, P, P, P, P, P, P, P], I),
             "tinfer_op_moe": ([I, I, I, I, I, I, I, P, P, P, P, P, P, P, I, P, P], I),
@@ -247,6 +248,11 @@ def tinfer_op_attention_noalloc(nq, nkv, d, max_ctx, theta, pos, n_chunks, qkv, 
     return lib().tinfer_op_attention_noalloc(nq, nkv, d, max_ctx, float(theta), pos, n_chunks,
                                              _ptr(qkv), _ptr(k_layer), _ptr(v_layer), _ptr(out),
                                              _stream(stream))
+
+
+def tinfer_op_gemv_batch(fmt, group, scale_dtype, rows, cols, m, packed, x, bias, epilogue, y, stream=None) -> int:
+    return lib().tinfer_op_gemv_batch(fmt, group, scale_dtype, rows, cols, m, _ptr(packed), _ptr(x), _ptr(bias),
+                                      epilogue, _ptr(y), _stream(stream))
 
 
 def tinfer_moe_packed_bytes(fmt, group, n_experts, hidden, ffn_e, which) -> int:

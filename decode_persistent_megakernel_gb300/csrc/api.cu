@@ -880,6 +880,45 @@ tinfer_status tinfer_op_attention(int nq, int nkv, int d, int max_ctx, double th
   return rc;
 }
 
+tinfer_status tinfer_op_gemv_batch(int fmt, int group, int scale_dtype, int rows, int cols, int m,
+                                   const void* packed_dev, const float* x_dev, const float* bias_dev,
+                                   int epilogue, float* y_dev, void* stream) {
+  const size_t rb = packed_row_bytes(fmt, cols, group);
+  if (rows <= 0 || rb == 0 || !packed_dev || !x_dev || !y_dev) return TINFER_ERR_INVALID_ARG;
+  if (epilogue != TINFER_EPI_STORE && epilogue != TINFER_EPI_RESIDUAL) return TINFER_ERR_INVALID_ARG;
+  if (m != 1 && m != 2 && m != 4 && m != 8) return TINFER_ERR_UNSUPPORTED;
+  for (const void* ptr : {packed_dev, (const void*)x_dev})
+    if (reinterpret_cast<uintptr_t>(ptr) & 15) return TINFER_ERR_INVALID_ARG;
+  // segments: a lane holds 8 / m units of 8 inputs of every vector, so a segment spans at most
+  // 2048 / m inputs; int4 segments hold whole groups of a lane's 8 / m consecutive words
+  int nseg = 1;
+  while (nseg < NCW && cols / nseg > 2048 / m) nseg *= 2;
+  const int ks = cols / nseg, unit = fmt == TINFER_INT4 ? 8 * (8 / m) : 8;
+  if (cols % nseg || ks > 2048 / m || ks % unit) return TINFER_ERR_UNSUPPORTED;
+  int dev = 0, sms = 0;
+  TRY_CUDA(cudaGetDevice(&dev));
+  TRY_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  TRY(op_scratch());
+  OpGemvMParams q{};
+  q.w = (const uint8_t*)packed_dev; q.rows = rows; q.cols = cols; q.rb = (int)rb;
+  q.fmt = fmt; q.group = group; q.scale_bf16 = scale_dtype == TINFER_SCALE_BF16;
+  q.m = m; q.nseg = nseg; q.x = x_dev; q.bias = bias_dev; q.y = y_dev;
+  q.residual = epilogue == TINFER_EPI_RESIDUAL; q.err = g_op.err; q.timeout_ns = DEFAULT_TIMEOUT_NS;
+  q.stages = 4;
+  q.slot = (int)std::max<size_t>(SLOT_MIN, align_up(rb * (size_t)(NCW / nseg), 1024));
+  size_t smem = smem_for(q.stages, q.slot, (int)align_up((size_t)m * cols * 4, 128));
+  while (smem > 227 * 1024 && q.stages > 2) smem = smem_for(--q.stages, q.slot, (int)align_up((size_t)m * cols * 4, 128));
+  if (smem > 227 * 1024) return TINFER_ERR_UNSUPPORTED;
+  // enough CTAs that one CTA's row results fit its shared row buffer
+  int grid = rows < sms ? rows : sms;
+  const int per = ROWV_MAX / (nseg * m) - 1;
+  if (per < 1) return TINFER_ERR_UNSUPPORTED;
+  if ((rows + per - 1) / per > grid) grid = (rows + per - 1) / per;
+  TRY_CUDA(set_smem_op_gemv_m(fmt, m, smem));
+  TRY_CUDA(launch_op_gemv_m(q, grid, smem, (cudaStream_t)stream));
+  return TINFER_OK;
+}
+
 size_t tinfer_moe_packed_bytes(int fmt, int group, int n_experts, int hidden, int ffn_e, int which) {
   if (n_experts <= 0) return 0;
   const size_t rbh = packed_row_bytes(fmt, hidden, group), rbf = packed_row_bytes(fmt, ffn_e, group);

@@ -92,6 +92,49 @@ __global__ void __launch_bounds__(NTHREADS, 1) op_attention_kernel(const __grid_
   __syncthreads();
 }
 
+// GEMV over a batch of MV vectors (the verify shape): the same ring and producer as the one-vector
+// GEMV, the batched consumer gemv_rows_m.
+template <int FMT, int MV>
+__global__ void __launch_bounds__(NTHREADS, 1) op_gemv_m_kernel(const __grid_constant__ OpGemvMParams q) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  Pipe pp;
+  pipe_init(pp, smem, q.stages, q.slot, q.timeout_ns, q.err, nullptr);
+  pipe_setup(pp);
+  __syncthreads();
+  const GemvDesc g{q.w, q.rows, q.cols, q.rb, q.fmt, q.group, q.scale_bf16, 1};
+  RowSplit rs = row_split(g, blockIdx.x, gridDim.x, q.slot);
+  const int wg = NCW / q.nseg;
+  int fit = q.slot / q.rb;
+  if (fit > NR_MAX) fit = NR_MAX;
+  rs.nr = fit - fit % wg;
+  const int tid = threadIdx.x;
+  if (tid >= NCT) {
+    if (tid == NCT) {
+      bool dead = false;
+      produce_rows(pp, g, rs, policy_evict_first(), dead);
+      prod_drain(pp);
+    }
+  } else {
+    gemv_rows_m<FMT, MV>(pp, g, rs, GemvMArgs{q.x, q.y, q.bias, q.residual, q.nseg}, tid);
+    if (tid == 0) *reinterpret_cast<volatile int*>(&pp.ms->cons_done) = 1;
+  }
+  __syncthreads();
+}
+
+static const void* gemv_m_fn(int fmt, int m) {
+  switch (fmt * 16 + m) {
+    case 1: return (const void*)op_gemv_m_kernel<0, 1>;
+    case 2: return (const void*)op_gemv_m_kernel<0, 2>;
+    case 4: return (const void*)op_gemv_m_kernel<0, 4>;
+    case 8: return (const void*)op_gemv_m_kernel<0, 8>;
+    case 17: return (const void*)op_gemv_m_kernel<1, 1>;
+    case 18: return (const void*)op_gemv_m_kernel<1, 2>;
+    case 20: return (const void*)op_gemv_m_kernel<1, 4>;
+    case 24: return (const void*)op_gemv_m_kernel<1, 8>;
+  }
+  return nullptr;
+}
+
 // ------------------------------------------------------------------------------ gathered experts
 
 // The chosen expert ids in shared memory; an id outside [0, n_experts) reads expert 0 and is
@@ -370,6 +413,13 @@ cudaError_t set_smem_mega(size_t b, int fmt, int nchl) {
 cudaError_t set_smem_phase(size_t b, int fmt, int nchl) { return raise_limit(step_fn(fmt, nchl, 2), b); }
 cudaError_t set_smem_op_gemv(size_t b) { return raise_limit((const void*)op_gemv_kernel, b); }
 cudaError_t set_smem_op_moe(int fmt, int nchl, int phase, size_t b) { return raise_limit(moe_fn(fmt, nchl, phase), b); }
+cudaError_t set_smem_op_gemv_m(int fmt, int m, size_t b) { return raise_limit(gemv_m_fn(fmt, m), b); }
+cudaError_t launch_op_gemv_m(const OpGemvMParams& q, int grid, size_t smem, cudaStream_t st) {
+  const void* fn = gemv_m_fn(q.fmt, q.m);
+  if (!fn) return cudaErrorInvalidDeviceFunction;
+  void* args[] = {const_cast<OpGemvMParams*>(&q)};
+  return cudaLaunchKernel(fn, dim3(grid), dim3(NTHREADS), args, smem, st);
+}
 cudaError_t launch_op_moe(const OpMoeParams& q, int phase, int grid, size_t smem, cudaStream_t st) {
   const void* fn = moe_fn(q.fmt, q.nchl, phase);
   if (!fn) return cudaErrorInvalidDeviceFunction;

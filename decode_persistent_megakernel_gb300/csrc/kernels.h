@@ -63,6 +63,23 @@ struct OpMoeParams {
   long long timeout_ns;
 };
 cudaError_t launch_op_moe(const OpMoeParams& q, int phase, int grid, size_t smem, cudaStream_t st);
+
+// GEMV over a batch of m activation vectors (op_gemv_m_kernel).
+struct OpGemvMParams {
+  const uint8_t* w;
+  int rows, cols, rb;
+  int fmt, group, scale_bf16;
+  int m, nseg;
+  const float* x;      // [m][cols]
+  const float* bias;   // [rows] or null
+  float* y;            // [m][rows]
+  int residual;
+  int* err;
+  int stages, slot;
+  long long timeout_ns;
+};
+cudaError_t launch_op_gemv_m(const OpGemvMParams& q, int grid, size_t smem, cudaStream_t st);
+cudaError_t set_smem_op_gemv_m(int fmt, int m, size_t bytes);
 cudaError_t set_smem_op_moe(int fmt, int nchl, int phase, size_t bytes);
 
 cudaError_t launch_megakernel(const StepParams& p, size_t smem, cudaStream_t st);

@@ -902,6 +902,156 @@ __device__ __forceinline__ bool colsplit_down(Pipe& pp, const GemvPlan& pl, cons
   return !*reinterpret_cast<volatile int*>(&ms->abort);
 }
 
+// GEMV over MV activation vectors at once, the verify shape of speculative decoding (flint,
+// "speculative decode": the megakernel verifies K + 1 tokens in one launch with the weights read
+// once): y[j][r] = sum_c W[r][c] x[j][c] for j < MV, fp32 accumulation. A lane keeps the
+// activations of all MV vectors for its part of a row segment in registers (NCH = 8 / MV units of
+// 8 inputs: 16-byte bf16 chunks, or 4-byte int4 words), so a row segment holds at most 2048 / MV
+// inputs and the weights of a row are decoded once for all MV vectors. int4 words are decoded in
+// place as for one vector (2^23 + q 16^i, activations pre-multiplied by 16^-i), with the zero
+// point subtracted exactly as 2^23 + 8 16^i and the scale applied to the decoded values, so each
+// product is (q - 8) s x rounded once. Row partials of 8 / MV rows ride in one window and meet in
+// one transposed reduction; the epilogue sums a row's segments in order (STORE with an optional
+// row bias, or RESIDUAL: y += .).
+struct GemvMArgs {
+  const float* x;      // [MV][cols]
+  float* y;            // [MV][rows]
+  const float* bias;   // [rows] or null
+  int residual;
+  int nseg;            // segments per row (a power of two dividing NCW)
+};
+template <int FMT, int MV>
+__device__ __forceinline__ bool gemv_rows_m(Pipe& pp, const GemvDesc& g, const RowSplit& rs, const GemvMArgs& q,
+                                            int tid) {
+  constexpr int NCH = 8 / MV;    // units per lane and segment
+  Misc* ms = pp.ms;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int nseg = q.nseg, ks = g.cols / nseg, us = ks / 8;  // inputs and units per segment
+  const int seg = warp % nseg, grp = warp / nseg, WG = NCW / nseg;
+  const int nrows = rs.r1 - rs.r0;
+  // the MV input vectors into shared memory, then this lane's units into registers
+  float* xs = sptr_w<float>(pp.xs);
+  for (int i = tid; i < MV * g.cols / 4; i += NCT)
+    reinterpret_cast<float4*>(xs)[i] = __ldcg(reinterpret_cast<const float4*>(q.x) + i);
+  named_sync(BAR_CONS, NCT);
+  // unit k of the lane: bf16 u = lane + 32 k (lanes read consecutive 16-byte chunks); int4
+  // u = lane * NCH + k (a lane's words are consecutive: one vector load)
+  float a[MV][NCH][8];
+#pragma unroll
+  for (int k = 0; k < NCH; ++k) {
+    const int u = FMT == 0 ? lane + 32 * k : lane * NCH + k;
+    const bool ok = u < us;
+    const int uc = ok ? u : 0;
+#pragma unroll
+    for (int j = 0; j < MV; ++j) {
+      const float* src = xs + j * g.cols + seg * ks + uc * 8;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float v = ok ? src[e] : 0.f;
+        a[j][k][e] = FMT == 0 ? v : v * ((e & 3) == 0 ? 1.f : (e & 3) == 1 ? 0.0625f : (e & 3) == 2 ? 0.00390625f : 0.000244140625f);
+      }
+    }
+  }
+  const uint32_t mag = opaque_u32(0x4B000000u);
+  const float2 B01 = make_float2(-8388616.f, -8388736.f);    // -(2^23 + 8 * 16^i), i = 0, 1
+  const float2 B23 = make_float2(-8390656.f, -8421376.f);    // i = 2, 3
+  const uint32_t seg_off = FMT == 0 ? (uint32_t)(seg * ks * 2) : (uint32_t)(seg * ks / 2);
+  const int m = rs.nr > grp ? (rs.nr - grp + WG - 1) / WG : 0;  // rows of the warp per full stage
+  constexpr int R = 8 / MV;                                     // rows per reduction window
+  float w[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) w[e] = 0.f;
+  int rl[R];
+  int filled = 0, nrow = 0;
+  auto flush = [&]() {
+    const float v = transpose_reduce8(w, lane);
+    const int qv = transpose_row8(lane), rr = qv / MV, j = qv % MV;
+    if ((lane & 3) == 0 && rr < filled) ms->rowv[(rl[rr] * nseg + seg) * MV + j] = v;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) w[e] = 0.f;
+    filled = 0;
+  };
+  for (int s0 = rs.r0; s0 < rs.r1; s0 += rs.nr) {
+    const int nrs = min(rs.nr, rs.r1 - s0);
+    const uint32_t st = cons_acquire(pp);
+#pragma unroll 1
+    for (int i = grp; i < nrs; i += WG) {
+      const uint32_t rowp = st + (uint32_t)i * g.rb + seg_off;
+      float2 acc[MV];
+#pragma unroll
+      for (int j = 0; j < MV; ++j) acc[j] = make_float2(0.f, 0.f);
+      if (FMT == 0) {
+#pragma unroll
+        for (int k = 0; k < NCH; ++k) {
+          const int u = min(lane + 32 * k, us - 1);
+          const uint4 wv = lds128(rowp + (uint32_t)u * 16u);
+          const float2 p0 = make_float2(bf16_lo(wv.x), bf16_hi(wv.x)), p1 = make_float2(bf16_lo(wv.y), bf16_hi(wv.y));
+          const float2 p2 = make_float2(bf16_lo(wv.z), bf16_hi(wv.z)), p3 = make_float2(bf16_lo(wv.w), bf16_hi(wv.w));
+#pragma unroll
+          for (int j = 0; j < MV; ++j) {
+            acc[j] = fma2(p0, make_float2(a[j][k][0], a[j][k][1]), acc[j]);
+            acc[j] = fma2(p1, make_float2(a[j][k][2], a[j][k][3]), acc[j]);
+            acc[j] = fma2(p2, make_float2(a[j][k][4], a[j][k][5]), acc[j]);
+            acc[j] = fma2(p3, make_float2(a[j][k][6], a[j][k][7]), acc[j]);
+          }
+        }
+      } else {
+        const int u0 = lane * NCH < us ? lane * NCH : 0;  // a lane past the segment reads word 0 (zero activations)
+        uint32_t wd[NCH];
+        if (NCH == 4) {
+          const uint4 v = lds128(rowp + (uint32_t)u0 * 4u);
+          wd[0] = v.x; wd[NCH > 1 ? 1 : 0] = v.y; wd[NCH > 2 ? 2 : 0] = v.z; wd[NCH > 3 ? 3 : 0] = v.w;
+        } else {
+#pragma unroll
+          for (int k = 0; k < NCH; ++k) wd[k] = lds32(rowp + (uint32_t)(u0 + k) * 4u);
+        }
+#pragma unroll
+        for (int k = 0; k < NCH; ++k) {
+          const int col = seg * ks + (u0 + k) * 8;
+          const uint16_t sb = lds16(st + (uint32_t)i * g.rb + (uint32_t)(g.cols / 2) + 2u * (uint32_t)(col / g.group));
+          const float sc = g.scale_bf16 ? bf16_to_f(sb) : __half2float(__ushort_as_half(sb));
+          const float2 s2 = make_float2(sc, sc);
+          const uint32_t lo = wd[k], hi = wd[k] >> 16;
+          const float2 d01 = __fmul2_rn(add2(make_float2(__uint_as_float(and_or<0x000Fu>(lo, mag)), __uint_as_float(and_or<0x00F0u>(lo, mag))), B01), s2);
+          const float2 d23 = __fmul2_rn(add2(make_float2(__uint_as_float(and_or<0x0F00u>(lo, mag)), __uint_as_float(and_or<0xF000u>(lo, mag))), B23), s2);
+          const float2 d45 = __fmul2_rn(add2(make_float2(__uint_as_float(and_or<0x000Fu>(hi, mag)), __uint_as_float(and_or<0x00F0u>(hi, mag))), B01), s2);
+          const float2 d67 = __fmul2_rn(add2(make_float2(__uint_as_float(and_or<0x0F00u>(hi, mag)), __uint_as_float(and_or<0xF000u>(hi, mag))), B23), s2);
+#pragma unroll
+          for (int j = 0; j < MV; ++j) {
+            acc[j] = fma2(d01, make_float2(a[j][k][0], a[j][k][1]), acc[j]);
+            acc[j] = fma2(d23, make_float2(a[j][k][2], a[j][k][3]), acc[j]);
+            acc[j] = fma2(d45, make_float2(a[j][k][4], a[j][k][5]), acc[j]);
+            acc[j] = fma2(d67, make_float2(a[j][k][6], a[j][k][7]), acc[j]);
+          }
+        }
+      }
+      // the row's MV partials enter the window at slots filled * MV + j
+      const int n = nrow++;
+      const int rlocal = (n / m) * rs.nr + grp + (n % m) * WG;
+#pragma unroll
+      for (int rr = 0; rr < R; ++rr)
+        if (rr == filled) {
+          rl[rr] = rlocal;
+#pragma unroll
+          for (int j = 0; j < MV; ++j) w[rr * MV + j] = acc[j].x + acc[j].y;
+        }
+      if (++filled == R) flush();
+    }
+    cons_release(pp, lane);
+  }
+  if (filled) flush();
+  named_sync(BAR_CONS, NCT);
+  for (int t = tid; t < nrows * MV; t += NCT) {
+    const int row = t / MV, j = t - row * MV, r = rs.r0 + row;
+    float v = 0.f;
+    for (int s2 = 0; s2 < nseg; ++s2) v += ms->rowv[(row * nseg + s2) * MV + j];
+    float* out = q.y + (size_t)j * g.rows + r;
+    if (q.residual) *out = __ldcg(out) + v;
+    else *out = q.bias ? q.bias[r] + v : v;
+  }
+  return !*reinterpret_cast<volatile int*>(&ms->abort);
+}
+
 // Dispatch to the instance of the weight format and chunk count per lane (rounded up to even).
 __device__ __forceinline__ bool gemv_consume_any(Pipe& pp, const GemvPlan& pl, Best& best, int tid,
                                                  unsigned long long* tr_ready) {

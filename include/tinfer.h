@@ -248,6 +248,18 @@ tinfer_status tinfer_op_gemv(int weight_format, int group_size, int scale_dtype,
                              double rms_eps, const float* bias_dev, int epilogue, float* y_dev,
                              int32_t* argmax_dev, void* stream);
 
+/* The same streaming GEMV over a batch of m activation vectors (m in {1, 2, 4, 8}), the verify
+ * shape of speculative decoding (flint, "speculative decode": K + 1 positions verified in one launch,
+ * the weights read once): y[j][r] = sum_c W[r][c] x[j][c] for j < m, fp32 accumulation, each int4
+ * weight decoded once for all m vectors. x_dev: fp32 [m][cols], y_dev: fp32 [m][rows] (both
+ * row-major), bias_dev: fp32 [rows] or NULL. epilogue: TINFER_EPI_STORE (y = W x + bias) or
+ * TINFER_EPI_RESIDUAL (y += W x). A row is cut into at most 8 segments of at most 2048 / m inputs
+ * (int4: whole runs of 8 / m words), so m * cols <= 16384; other shapes return
+ * TINFER_ERR_UNSUPPORTED. Asynchronous on `stream`. */
+tinfer_status tinfer_op_gemv_batch(int weight_format, int group_size, int scale_dtype, int rows, int cols,
+                                   int m, const void* packed_dev, const float* x_dev,
+                                   const float* bias_dev, int epilogue, float* y_dev, void* stream);
+
 /* Attention for one layer at position pos: qkv_dev holds the raw projections [q (n_heads*head_dim) |
  * k (n_kv_heads*head_dim) | v (n_kv_heads*head_dim)] in fp32 (bias already added). The op applies
  * RoPE (fp32 cos/sin table built on the host in double from rope_theta) to q and k, writes
