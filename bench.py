@@ -224,6 +224,71 @@ def oracle_baseline(c, w, K, V, budget_s: float):
                       f"{el1:.1f} s"}
 
 
+def ops_measurements(T, torch, peak):
+    """Device-timed rates of the op-level paths on inputs larger than L2, as GB/s of the weight bytes
+    each call must read: the gathered-expert MLP (64 experts, 8 chosen, hidden 2048, expert FFN
+    1024; successive calls route to disjoint expert sets, 805 MB of bf16 experts in all) and the
+    batched GEMV at m = 1, 2, 4, 8 over four 16384 x 2048 bf16 matrices taken in turn."""
+    out = {}
+    st = torch.cuda.current_stream()
+
+    def timed(fn, n):
+        for i in range(3):
+            fn(i)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        for i in range(n):
+            fn(i)
+        b.record(st)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+
+    for fmt, group in (("bf16", 64), ("int4", 64)):
+        E, k, H, F = 64, 8, 2048, 1024
+        m = synth.make_moe(E, k, H, F, fmt, group, "fp16", seed=0)
+        f = T.TINFER_INT4 if fmt == "int4" else T.TINFER_BF16
+        dev = {n: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).cuda()
+               for n, v in m.items() if v is not None and n[0] in "ws" and n != "weights"}
+        gu = torch.empty(T.tinfer_moe_packed_bytes(f, group, E, H, F, 0), dtype=torch.uint8, device="cuda")
+        dn = torch.empty(T.tinfer_moe_packed_bytes(f, group, E, H, F, 1), dtype=torch.uint8, device="cuda")
+        assert T.tinfer_pack_moe(f, group, 0, E, H, F, dev["wg"], dev.get("sg"), dev["wu"], dev.get("su"),
+                                 dev["wd"], dev.get("sd"), gu, dn) == 0
+        del dev
+        ids = [torch.arange(8 * i, 8 * i + 8, dtype=torch.int32, device="cuda") for i in range(E // k)]
+        wts = torch.tensor(m["weights"], device="cuda")
+        x = torch.tensor(m["x"], device="cuda")
+        h = torch.empty(k * F, device="cuda")
+        y = torch.empty(H, device="cuda")
+        ms = timed(lambda i: T.tinfer_op_moe(f, group, 0, E, k, H, F, gu, dn, ids[i % len(ids)], wts, x, h, y,
+                                             0, None, st), 64)
+        nbytes = (gu.numel() + dn.numel()) * k // E
+        out[f"moe_{fmt}"] = {"shape": f"{E} experts, top {k}, hidden {H}, expert ffn {F}", "us_per_call": ms * 1e3,
+                             "weight_bytes": nbytes, "achieved_gbs": nbytes / (ms * 1e-3) / 1e9,
+                             "frac": nbytes / (ms * 1e-3) / 1e9 / peak}
+        del gu, dn
+        torch.cuda.empty_cache()
+    rows, cols = 16384, 2048
+    mats = []
+    for i in range(4):
+        W = synth.normal_bf16(f"bench.gemvm.{i}", (rows, cols), 0.0, 0.02, 0)
+        pk = torch.empty(rows * cols * 2, dtype=torch.uint8, device="cuda")
+        assert T.tinfer_pack_matrix(0, 64, 0, rows, cols, torch.from_numpy(W.view(np.int16)).cuda(), None, pk) == 0
+        mats.append(pk)
+    res = {}
+    for mv in (1, 2, 4, 8):
+        xs = torch.randn(mv * cols, device="cuda")
+        ys = torch.empty(mv * rows, device="cuda")
+        ms = timed(lambda i: T.tinfer_op_gemv_batch(0, 64, 0, rows, cols, mv, mats[i % 4], xs, None, 0, ys, st), 64)
+        nb = rows * cols * 2
+        res[str(mv)] = {"us_per_call": ms * 1e3, "achieved_gbs": nb / (ms * 1e-3) / 1e9,
+                        "frac": nb / (ms * 1e-3) / 1e9 / peak}
+    out["gemv_batch_bf16_16384x2048"] = res
+    del mats
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_reference(args):
     """The reference arm: the CPU oracle timed on the host cores, same config and metric."""
     rank = int(os.environ.get("RANK", "0"))
@@ -271,6 +336,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-loop", action="store_true", help="skip the in-kernel token loop measurement")
+    ap.add_argument("--no-ops", action="store_true", help="skip the op-level measurements (MoE, batched GEMV)")
     ap.add_argument("--sync", default="stamps", choices=["stamps", "barrier"],
                     help="how a phase waits for the one before it (persistent kernel)")
     ap.add_argument("--ffn-split", action="store_true",
@@ -384,6 +450,10 @@ def main():
         del eng
         torch.cuda.empty_cache()
 
+    ops = None
+    if not args.no_ops and rank == 0:
+        ops = ops_measurements(T, torch, measured_peaks()[0])
+
     # a pure streaming-read probe (page 1's yardstick), same process
     read_gbs = None
     try:
@@ -456,6 +526,8 @@ def main():
         "launch": {"grid": r["grid"], "threads": r["threads"], "smem": r["smem"], "ring_stages": r["stages"],
                    "slot_bytes": r["slot"]},
     }
+    if ops is not None:
+        line["ops"] = ops
     if "loop" in results:
         lp = results["loop"]
         line["token_loop"] = {"tokens/s": world * 1e3 / lp["ms_token"], "ms_per_token": lp["ms_token"],

@@ -911,7 +911,7 @@ tinfer_status tinfer_op_gemv_batch(int fmt, int group, int scale_dtype, int rows
   if (smem > 227 * 1024) return TINFER_ERR_UNSUPPORTED;
   // enough CTAs that one CTA's row results fit its shared row buffer
   int grid = rows < sms ? rows : sms;
-  const int per = ROWV_MAX / (nseg * m) - 1;
+  const int per = std::max(ROWV_MAX, m * cols) / (nseg * m) - 1;  // row results: the larger buffer
   if (per < 1) return TINFER_ERR_UNSUPPORTED;
   if ((rows + per - 1) / per > grid) grid = (rows + per - 1) / per;
   TRY_CUDA(set_smem_op_gemv_m(fmt, m, smem));

@@ -952,6 +952,10 @@ __device__ __forceinline__ bool gemv_rows_m(Pipe& pp, const GemvDesc& g, const R
       }
     }
   }
+  // once every warp holds its activations, the input buffer (m * cols floats) takes the row results
+  // when it is the larger of the two buffers
+  named_sync(BAR_CONS, NCT);
+  float* rowv = MV * g.cols > ROWV_MAX ? xs : ms->rowv;
   const uint32_t mag = opaque_u32(0x4B000000u);
   const float2 B01 = make_float2(-8388616.f, -8388736.f);    // -(2^23 + 8 * 16^i), i = 0, 1
   const float2 B23 = make_float2(-8390656.f, -8421376.f);    // i = 2, 3
@@ -966,7 +970,7 @@ __device__ __forceinline__ bool gemv_rows_m(Pipe& pp, const GemvDesc& g, const R
   auto flush = [&]() {
     const float v = transpose_reduce8(w, lane);
     const int qv = transpose_row8(lane), rr = qv / MV, j = qv % MV;
-    if ((lane & 3) == 0 && rr < filled) ms->rowv[(rl[rr] * nseg + seg) * MV + j] = v;
+    if ((lane & 3) == 0 && rr < filled) rowv[(rl[rr] * nseg + seg) * MV + j] = v;
 #pragma unroll
     for (int e = 0; e < 8; ++e) w[e] = 0.f;
     filled = 0;
@@ -1044,7 +1048,7 @@ __device__ __forceinline__ bool gemv_rows_m(Pipe& pp, const GemvDesc& g, const R
   for (int t = tid; t < nrows * MV; t += NCT) {
     const int row = t / MV, j = t - row * MV, r = rs.r0 + row;
     float v = 0.f;
-    for (int s2 = 0; s2 < nseg; ++s2) v += ms->rowv[(row * nseg + s2) * MV + j];
+    for (int s2 = 0; s2 < nseg; ++s2) v += rowv[(row * nseg + s2) * MV + j];
     float* out = q.y + (size_t)j * g.rows + r;
     if (q.residual) *out = __ldcg(out) + v;
     else *out = q.bias ? q.bias[r] + v : v;
