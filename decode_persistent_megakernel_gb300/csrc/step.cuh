@@ -473,6 +473,14 @@ __device__ __forceinline__ float fetch_vector_n(Pipe& pp, const ActSrc& src, int
   float ss = 0.f;
   for (int j0 = tid; j0 < nb; j0 += IF * NCT) {
     float4 x[IF];
+    // the gains do not depend on the previous phase: their loads issue first, so that their
+    // latency hides under the wait for the stamped input instead of following it
+    float4 gv[IF];
+#pragma unroll
+    for (int u = 0; u < IF; ++u) {
+      const int j = j0 + u * NCT;
+      gv[u] = norm && j < nb ? gain_block(src, j) : make_float4(1.f, 1.f, 1.f, 1.f);
+    }
     if (src.xw) {
       // two 16-byte loads per block of 4 stamped words; stale blocks are read again until their
       // writers' stamps show (bounded)
@@ -546,8 +554,7 @@ __device__ __forceinline__ float fetch_vector_n(Pipe& pp, const ActSrc& src, int
         ss = fmaf(x[u].y, x[u].y, ss);
         ss = fmaf(x[u].z, x[u].z, ss);
         ss = fmaf(x[u].w, x[u].w, ss);
-        float4 g = make_float4(1.f, 1.f, 1.f, 1.f);
-        if (norm) g = gain_block(src, j);
+        const float4 g = gv[u];
         xs[j] = make_float4(x[u].x * g.x, x[u].y * g.y, x[u].z * g.z, x[u].w * g.w);
       }
     }
