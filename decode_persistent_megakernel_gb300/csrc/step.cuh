@@ -465,11 +465,25 @@ __device__ __forceinline__ float4 gain_block(const ActSrc& src, int j) {
 // way; the return value is 1 / rms(x) (1 without a norm), the same in every consumer thread.
 // Returns after the named barrier that publishes the copy; the CTA's abort flag is then set (the
 // same in every thread) if a stamped source never showed up.
+// Layout in shared memory, for the GEMV's 16-byte weight chunks of E inputs (E = 8 for bf16, 32 for
+// int4): the inputs of chunk C are its E / 4 float4 blocks, block b stored at C * E / 4 +
+// (b ^ chunk_swizzle(C)), so that the lanes of a quarter-warp, which read consecutive chunks, hit
+// distinct banks while every lane reads its blocks in order (no register shuffling). For int4 the
+// stored values are also pre-multiplied by 16^-(i mod 4) for input i of the chunk (exact: powers of
+// two), the activation scaling of the in-place nibble decode (dot32_int4).
+template <int E>
+__device__ __forceinline__ int chunk_swizzle(int c) {
+  return E == 8 ? (c >> 2) & 1 : c & (E / 4 - 1);
+}
 template <int IF>
-__device__ __forceinline__ float fetch_vector_n(Pipe& pp, const ActSrc& src, int tid) {
+__device__ __forceinline__ float fetch_vector_n(Pipe& pp, const ActSrc& src, int tid, int fmt) {
   const bool norm = src.gf || src.gb;
   const int nb = src.n / 4;
   float4* xs = sptr_w<float4>(pp.xs);
+  // block j is block j % B of chunk j / B (B = E / 4 blocks per chunk)
+  const int bsh = fmt == 1 ? 3 : 1;
+  const float4 pre = fmt == 1 ? make_float4(1.f, 0.0625f, 0.00390625f, 0.000244140625f)
+                              : make_float4(1.f, 1.f, 1.f, 1.f);
   float ss = 0.f;
   for (int j0 = tid; j0 < nb; j0 += IF * NCT) {
     float4 x[IF];
@@ -555,7 +569,10 @@ __device__ __forceinline__ float fetch_vector_n(Pipe& pp, const ActSrc& src, int
         ss = fmaf(x[u].z, x[u].z, ss);
         ss = fmaf(x[u].w, x[u].w, ss);
         const float4 g = gv[u];
-        xs[j] = make_float4(x[u].x * g.x, x[u].y * g.y, x[u].z * g.z, x[u].w * g.w);
+        const int c = j >> bsh, b = j & ((1 << bsh) - 1);
+        const int key = fmt == 1 ? chunk_swizzle<32>(c) : chunk_swizzle<8>(c);
+        xs[(c << bsh) + (b ^ key)] = make_float4(x[u].x * g.x * pre.x, x[u].y * g.y * pre.y,
+                                                 x[u].z * g.z * pre.z, x[u].w * g.w * pre.w);
       }
     }
   }
@@ -573,38 +590,14 @@ __device__ __forceinline__ float fetch_vector_n(Pipe& pp, const ActSrc& src, int
 
 
 
-// One lane's chunk of the input vector from the shared-memory copy: E / 4 consecutive 16-byte blocks
-// starting at block `blk0`. Lanes of a warp own chunks 32 or 128 bytes apart, so the blocks are
-// visited in a lane-rotated order (rotation lane % R, R = E / 4 for int4, 2 for bf16 with the
-// rotation switching at lane 4) that spreads a quarter-warp's loads over all banks; the blocks are
-// then rotated back into place in registers.
+// One lane's chunk C of the input vector from the shared-memory copy (fetch_vector_n's layout): its
+// E / 4 float4 blocks in order, each read from its swizzled place.
 template <int E>
-__device__ __forceinline__ void load_chunk(const float4* xs, int blk0, int lane, float4 (&v)[E / 4]) {
+__device__ __forceinline__ void load_chunk(const float4* xs, int c, float4 (&v)[E / 4]) {
   constexpr int B = E / 4;
-  if (B == 2) {
-    const int h = (lane >> 2) & 1;
-    const float4 p = xs[blk0 + h], q = xs[blk0 + (h ^ 1)];
-    v[0] = h ? q : p;
-    v[B - 1] = h ? p : q;
-  } else {
-    const int r = lane & (B - 1);
-    float4 t[B];
+  const int key = chunk_swizzle<E>(c);
 #pragma unroll
-    for (int b = 0; b < B; ++b) t[b] = xs[blk0 + ((b + r) & (B - 1))];
-    // t[b] holds block (b + r) mod B: rotate right by r to put block b at v[b]
-#pragma unroll
-    for (int sh = 1; sh < B; sh <<= 1) {
-      if (r & sh) {
-        float4 u[B];
-#pragma unroll
-        for (int b = 0; b < B; ++b) u[b] = t[(b - sh + B) & (B - 1)];
-#pragma unroll
-        for (int b = 0; b < B; ++b) t[b] = u[b];
-      }
-    }
-#pragma unroll
-    for (int b = 0; b < B; ++b) v[b] = t[b];
-  }
+  for (int b = 0; b < B; ++b) v[b] = xs[c * B + (b ^ key)];
 }
 
 // Everything a GEMV phase needs that does not depend on other CTAs' results of the previous phase:
@@ -657,7 +650,7 @@ __device__ __forceinline__ bool gemv_rows(Pipe& pp, const GemvPlan& pl, Best& be
   // Chunks past the segment read the segment's last chunk slot and are zeroed, so that the row loop
   // needs no per-lane branches
   if (tr_ready && tid == 0) tr_ready[TR_ENTRY - TR_READY] = globaltimer();
-  const float inv = fetch_vector_n<IF>(pp, src, tid);
+  const float inv = fetch_vector_n<IF>(pp, src, tid, FMT);
   if (tr_ready && tid == 0) tr_ready[TR_FETCHED - TR_READY] = globaltimer();
   if (*reinterpret_cast<volatile int*>(&pp.ms->abort)) return false;  // uniform after the fetch
   (void)norm;
@@ -670,7 +663,7 @@ __device__ __forceinline__ bool gemv_rows(Pipe& pp, const GemvPlan& pl, Best& be
       const bool ok = lane + 32 * k < si.chs;
       const int c = min(lane + 32 * k, si.chs - 1);  // clamped chunk: always a valid address
       float4 v[E / 4];
-      load_chunk<E>(xsv, (seg * si.ks + c * E) / 4, lane, v);
+      load_chunk<E>(xsv, (seg * si.ks) / E + c, v);
 #pragma unroll
       for (int b = 0; b < E / 4; ++b) {
         a[k][4 * b + 0] = ok ? v[b].x : 0.f;
@@ -682,15 +675,19 @@ __device__ __forceinline__ bool gemv_rows(Pipe& pp, const GemvPlan& pl, Best& be
   }
   if (tr_ready && tid == 0) tr_ready[TR_ACT - TR_READY] = globaltimer() + (unsigned long long)(a[0][0] * 0.f);
   if (FMT == 1) {
+    // the chunk's sum of (unscaled) inputs for the zero point, as a tree: the inputs arrive
+    // pre-multiplied by 16^-(i mod 4), and scaling back by the same powers of two is exact
 #pragma unroll
     for (int k = 0; k < NCHL; ++k) {
-      float t = 0.f;
+      float sb[E / 4];
 #pragma unroll
-      for (int e = 0; e < E; ++e) t += a[k][e];
-      S[k] = t;
+      for (int b = 0; b < E / 4; ++b)
+        sb[b] = fmaf(4096.f, a[k][4 * b + 3], fmaf(256.f, a[k][4 * b + 2], fmaf(16.f, a[k][4 * b + 1], a[k][4 * b])));
 #pragma unroll
-      for (int e = 0; e < E; ++e)
-        a[k][e] *= (e & 3) == 0 ? 1.f : (e & 3) == 1 ? 0.0625f : (e & 3) == 2 ? 0.00390625f : 0.000244140625f;
+      for (int w = E / 8; w >= 1; w >>= 1)
+#pragma unroll
+        for (int b = 0; b < w; ++b) sb[b] += sb[b + w];
+      S[k] = sb[0];
     }
   }
   if (tr_ready && tid == 0) *tr_ready = globaltimer();
