@@ -1610,55 +1610,75 @@ static __device__ bool attn_unit(Pipe& pp, const AttnArgs& A, const AttnSplit& s
 // (per = ceil(G * d / nch)), one warp per output, lanes over chunks, and writes them as stamped
 // words. No ticket: every unit waits only for its siblings' partials, and the whole merge is spread
 // over the head's units. Returns false (the same in every consumer thread) if partials never came.
-static __device__ bool attn_merge_slice(Pipe& pp, const AttnArgs& A, const AttnSplit& sp, int j, int c,
-                                        int tid, unsigned long long* tr = nullptr) {
+template <int MB>
+__device__ __forceinline__ bool attn_merge_slice_mb(Pipe& pp, const AttnArgs& A, const AttnSplit& sp, int j,
+                                                    int c, int tid, unsigned long long* tr) {
   const int G = A.nq / A.nkv, d = A.d, nch = sp.nch;
   const int lane = tid & 31, warp = tid >> 5;
   const int nout = G * d, per = (nout + nch - 1) / nch;
   const int o0 = c * per, o1 = min(o0 + per, nout);
   const unsigned sv = A.stamp_out;
   const bool check = A.check != 0;
-  // two outputs per warp and pass: all six loads of a chunk batch are issued before any is used,
-  // and every stale one is read again in the same turn until its sibling's stamp shows
+  // two outputs per warp and pass: the six loads of up to MB chunk batches (32 chunks each) are all
+  // issued before any is used, and every stale one is read again in the same turn until its
+  // sibling's stamp shows; the batches are then merged in order (the same arithmetic as one batch
+  // at a time, so the graph path's ticket merge still gives the same bits)
   for (int oa = o0 + warp; oa < o1; oa += 2 * NCW) {
     const int ob = oa + NCW;
     const bool hb = ob < o1;  // warp-uniform
     const int ga = oa / d, ia = oa - ga * d, ha = j * G + ga;
     const int gb = hb ? ob / d : ga, ib = hb ? ob - gb * d : ia, hb_ = j * G + gb;
     float Ma = -CUDART_INF_F, na = 0.f, da = 0.f, Mb = -CUDART_INF_F, nb = 0.f, db = 0.f;
-    for (int cb = 0; cb < nch; cb += 32) {
-      const int cc = cb + lane;
-      const bool on = cc < nch;
-      const size_t mia = (size_t)ha * A.nch_cap + cc, mib = (size_t)hb_ * A.nch_cap + cc;
-      const uint64_t* src[6] = {A.pmw + mia, A.plw + mia, A.pow_ + mia * d + ia,
-                                A.pmw + mib, A.plw + mib, A.pow_ + mib * d + ib};
-      const unsigned need = on ? (hb ? 0x3Fu : 0x07u) : 0u;
-      uint64_t w[6];
+    for (int cb0 = 0; cb0 < nch; cb0 += 32 * MB) {
+      uint64_t w[MB][6];
+      const uint64_t* src[MB][6];
+      unsigned need = 0;  // bit 6 * q + e: word e of batch q
 #pragma unroll
-      for (int e = 0; e < 6; ++e) w[e] = (need & (1u << e)) ? ld_relaxed_u64(src[e]) : 0;
+      for (int q = 0; q < MB; ++q) {
+        const int cc = cb0 + 32 * q + lane;
+        const bool on = cc < nch;
+        const int ca = on ? cc : nch - 1;  // addresses stay inside the partial buffers
+        const size_t mia = (size_t)ha * A.nch_cap + ca, mib = (size_t)hb_ * A.nch_cap + ca;
+        src[q][0] = A.pmw + mia; src[q][1] = A.plw + mia; src[q][2] = A.pow_ + mia * d + ia;
+        src[q][3] = A.pmw + mib; src[q][4] = A.plw + mib; src[q][5] = A.pow_ + mib * d + ib;
+        if (on) need |= (hb ? 0x3Fu : 0x07u) << (6 * q);
+#pragma unroll
+        for (int e = 0; e < 6; ++e) w[q][e] = (need >> (6 * q + e)) & 1u ? ld_relaxed_u64(src[q][e]) : 0;
+      }
       if (check) {
         unsigned stale = 0;
 #pragma unroll
-        for (int e = 0; e < 6; ++e)
-          if ((need & (1u << e)) && word_stamp(w[e]) != sv) stale |= 1u << e;
+        for (int q = 0; q < MB; ++q)
+#pragma unroll
+          for (int e = 0; e < 6; ++e)
+            if (((need >> (6 * q + e)) & 1u) && word_stamp(w[q][e]) != sv) stale |= 1u << (6 * q + e);
         Poll pl;
         while (stale && pl.again(pp)) {
 #pragma unroll
-          for (int e = 0; e < 6; ++e)
-            if (stale & (1u << e)) w[e] = ld_relaxed_u64(src[e]);
+          for (int q = 0; q < MB; ++q)
 #pragma unroll
-          for (int e = 0; e < 6; ++e)
-            if ((stale & (1u << e)) && word_stamp(w[e]) == sv) stale &= ~(1u << e);
+            for (int e = 0; e < 6; ++e)
+              if ((stale >> (6 * q + e)) & 1u) w[q][e] = ld_relaxed_u64(src[q][e]);
+#pragma unroll
+          for (int q = 0; q < MB; ++q)
+#pragma unroll
+            for (int e = 0; e < 6; ++e)
+              if (((stale >> (6 * q + e)) & 1u) && word_stamp(w[q][e]) == sv) stale &= ~(1u << (6 * q + e));
         }
       }
-      float ma = -CUDART_INF_F, la = 0.f, va = 0.f, mb = -CUDART_INF_F, lb = 0.f, vb = 0.f;
-      if (on) {
-        ma = word_value(w[0]); la = word_value(w[1]); va = word_value(w[2]);
-        if (hb) { mb = word_value(w[3]); lb = word_value(w[4]); vb = word_value(w[5]); }
+      if (tr && tid == 0 && cb0 == 0 && oa == o0) tr[TR_AUX1] = globaltimer();  // siblings' partials seen
+#pragma unroll
+      for (int q = 0; q < MB; ++q) {
+        if (cb0 + 32 * q >= nch) break;  // warp-uniform: the batches the one-at-a-time merge would run
+        const bool on = cb0 + 32 * q + lane < nch;
+        float ma = -CUDART_INF_F, la = 0.f, va = 0.f, mb = -CUDART_INF_F, lb = 0.f, vb = 0.f;
+        if (on) {
+          ma = word_value(w[q][0]); la = word_value(w[q][1]); va = word_value(w[q][2]);
+          if (hb) { mb = word_value(w[q][3]); lb = word_value(w[q][4]); vb = word_value(w[q][5]); }
+        }
+        merge_step(Ma, na, da, ma, la, va);
+        if (hb) merge_step(Mb, nb, db, mb, lb, vb);
       }
-      if (tr && tid == 0 && cb == 0 && oa == o0) tr[TR_AUX1] = globaltimer();  // siblings' partials seen
-      merge_step(Ma, na, da, ma, la, va);
-      if (hb) merge_step(Mb, nb, db, mb, lb, vb);
     }
     if (lane == 0) {
       st_relaxed_u64(A.outw + (size_t)ha * d + ia, stamp_word(na / da, A.stamp_out));
@@ -1667,6 +1687,16 @@ static __device__ bool attn_merge_slice(Pipe& pp, const AttnArgs& A, const AttnS
   }
   named_sync(BAR_CONS, NCT);
   return !*reinterpret_cast<volatile int*>(&pp.ms->abort);
+}
+
+// The merge with as many chunk batches in flight as the head has (up to four): one L2 round trip for
+// the partials of up to 128 chunks (the Qwen-shaped step: 76 chunks, 9 % faster than one batch at a
+// time), while heads of at most 32 chunks keep the one-batch code.
+static __device__ bool attn_merge_slice(Pipe& pp, const AttnArgs& A, const AttnSplit& sp, int j, int c,
+                                        int tid, unsigned long long* tr = nullptr) {
+  if (sp.nch <= 32) return attn_merge_slice_mb<1>(pp, A, sp, j, c, tid, tr);
+  if (sp.nch <= 64) return attn_merge_slice_mb<2>(pp, A, sp, j, c, tid, tr);
+  return attn_merge_slice_mb<4>(pp, A, sp, j, c, tid, tr);
 }
 
 }  // namespace tinfer
