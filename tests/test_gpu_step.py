@@ -70,11 +70,12 @@ def test_tiny_model_teacher_forced(mode):
     dict(weight_format="int4", group_size=64, scale_dtype="fp16", ffn=704),
     dict(weight_format="int4", group_size=128, scale_dtype="bf16", ffn=768, tied=True),
 ])
-def test_variants_teacher_forced(over):
+@pytest.mark.parametrize("mode", MODES)
+def test_variants_teacher_forced(over, mode):
     c = synth.config("tiny", n_layers=2, max_ctx=300, **over)
     w = synth.make_model(c, seed=1)
     # a prefilled cache so that attention spans several chunks
-    run_teacher_forced(c, w, T.TINFER_MEGAKERNEL, 1, 3, prefill=280, seed=1)
+    run_teacher_forced(c, w, mode, 1, 3, prefill=280, seed=1)
 
 
 def test_megakernel_and_graph_are_bitwise_equal_and_deterministic():
