@@ -20,7 +20,7 @@ TINFER_MEGAKERNEL, TINFER_GRAPH = 0, 1
 TINFER_Q_GRID, TINFER_Q_SMEM, TINFER_Q_RING_STAGES, TINFER_Q_SLOT_BYTES, TINFER_Q_KERNELS_PER_STEP, \
     TINFER_Q_TRACE_BYTES, TINFER_Q_BLOCK_THREADS = range(7)
 TINFER_EPI_STORE, TINFER_EPI_RESIDUAL, TINFER_EPI_SWIGLU, TINFER_EPI_ARGMAX = range(4)
-TINFER_S_INFLIGHT, TINFER_S_INFLIGHT_LM, TINFER_S_L2_LOOKAHEAD, TINFER_S_L2_PACE, TINFER_S_SYNC = range(5)
+TINFER_S_INFLIGHT, TINFER_S_INFLIGHT_LM, TINFER_S_L2_LOOKAHEAD, TINFER_S_L2_PACE, TINFER_S_SYNC, TINFER_S_ATTN_CHUNKS = range(6)
 TINFER_SYNC_STAMPS, TINFER_SYNC_GRID_BARRIER = 0, 1
 TINFER_NOALLOC_SCRATCH_BYTES = 1 << 20
 TRACE_FIELDS = 10  # stamps per CTA and phase of the timeline (tinfer_set_trace)

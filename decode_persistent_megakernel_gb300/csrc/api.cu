@@ -688,6 +688,17 @@ tinfer_status tinfer_set_schedule(tinfer_ctx* x, int knob, long long value) {
       if (value < 0 || value > MAX_STAGES) return TINFER_ERR_INVALID_ARG;
       p.inflight_lm = (int)value;
       break;
+    case TINFER_S_ATTN_CHUNKS: {
+      // 0: the automatic split; n: every chunk must still fit one ring slot at max_ctx (n at least
+      // the automatic split's minimum) and the partial buffers hold at most nch_cap chunks
+      if (value == 0) { p.n_chunks_override = 0; break; }
+      int tmax = p.slot_bytes / (2 * p.m.d);
+      if (tmax > T_MAX) tmax = T_MAX;
+      const long long nmin = (p.m.max_ctx + tmax - 1) / tmax;
+      if (value < nmin || value > p.nch_cap) return TINFER_ERR_INVALID_ARG;
+      p.n_chunks_override = (int)value;
+      break;
+    }
     case TINFER_S_SYNC:
       if (value != TINFER_SYNC_STAMPS && value != TINFER_SYNC_GRID_BARRIER) return TINFER_ERR_INVALID_ARG;
       if (x->cfg.exec_mode != TINFER_MEGAKERNEL) return TINFER_ERR_UNSUPPORTED;
@@ -714,6 +725,7 @@ long long tinfer_get_schedule(const tinfer_ctx* x, int knob) {
     case TINFER_S_SYNC: return x->p.sync_barrier;
     case TINFER_S_INFLIGHT: return x->p.inflight;
     case TINFER_S_INFLIGHT_LM: return x->p.inflight_lm;
+    case TINFER_S_ATTN_CHUNKS: return x->p.n_chunks_override;
   }
   return -1;
 }

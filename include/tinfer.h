@@ -210,7 +210,14 @@ tinfer_status tinfer_debug_withhold_results(tinfer_ctx* ctx, int cta, int phase)
  * Takes effect from the next step; results do not depend on it. tinfer_get_schedule returns the
  * current value, or -1 for an unknown knob. */
 enum { TINFER_S_INFLIGHT = 0, TINFER_S_INFLIGHT_LM = 1, TINFER_S_L2_LOOKAHEAD = 2, TINFER_S_L2_PACE = 3,
-       TINFER_S_SYNC = 4 };
+       TINFER_S_SYNC = 4, TINFER_S_ATTN_CHUNKS = 5 };
+/* TINFER_S_ATTN_CHUNKS: chunks per KV head of the split-K attention ("One launch per token", "The
+ * attention trap": split the context across the SMs, then combine). 0 (default): the automatic
+ * split, enough chunks that the (KV head, chunk) units cover the grid; n > 0: n chunks of
+ * ceil((pos + 1) / n) positions at every position (chunks past the context are empty and weigh 0).
+ * n must be at least the number of chunks that keeps every chunk within one ring slot at max_ctx
+ * and at most the automatic split's count at max_ctx (the partial buffers' capacity), else
+ * TINFER_ERR_INVALID_ARG. Results change only by the order of the combine's additions. */
 /* TINFER_S_SYNC: how a phase waits for the one before it. TINFER_SYNC_STAMPS (default): each CTA
  * waits only for the stamped results it reads. TINFER_SYNC_GRID_BARRIER: every CTA also passes a
  * grid barrier before every phase ("Decoding in tiles", section 4: every wave ends at a grid

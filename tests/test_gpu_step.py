@@ -244,3 +244,32 @@ def test_grid_barrier_schedule_reports_a_withheld_result():
     eng = T.Engine(c, w, T.TINFER_GRAPH)
     assert T.tinfer_set_schedule(eng.ctx, T.TINFER_S_SYNC, T.TINFER_SYNC_GRID_BARRIER) == T.TINFER_ERR_UNSUPPORTED
     eng.close()
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_fixed_attention_chunk_counts_match_oracle(mode):
+    """TINFER_S_ATTN_CHUNKS: a fixed number of split-K chunks per KV head (empty chunks at short
+    contexts included) gives the oracle's step; values that would overflow a ring slot at max_ctx or
+    the partial buffers are rejected on the host."""
+    c = synth.config("tiny", max_ctx=300)
+    w = synth.make_model(c, seed=7)
+    K, V = synth.make_kv(c, 270, seed=7)
+    eng = T.Engine(c, w, mode, kv=(K, V))
+    auto = T.tinfer_get_schedule(eng.ctx, T.TINFER_S_ATTN_CHUNKS)
+    assert auto == 0
+    assert T.tinfer_set_schedule(eng.ctx, T.TINFER_S_ATTN_CHUNKS, 1) == T.TINFER_ERR_INVALID_ARG
+    assert T.tinfer_set_schedule(eng.ctx, T.TINFER_S_ATTN_CHUNKS, 100000) == T.TINFER_ERR_INVALID_ARG
+    om = ORC.model(c, w)
+    toks = synth.make_tokens(c, 6, seed=7)
+    for k, (n, t) in enumerate(zip([2, 5, 33, 2, 76, 0], toks.tolist())):
+        assert T.tinfer_set_schedule(eng.ctx, T.TINFER_S_ATTN_CHUNKS, n) == 0
+        assert T.tinfer_get_schedule(eng.ctx, T.TINFER_S_ATTN_CHUNKS) == n
+        eng.step(t, 270 + k)
+        torch.cuda.synchronize()
+        ref, am, rc = ORC.decode_step(om, t, 270 + k, K, V)
+        err, rel, margin = compare_logits(eng.logits.cpu().numpy(), ref)
+        assert err <= LOGIT_MAX_ABS and rel <= LOGIT_REL_L2, (n, k, err, rel)
+        if margin > ARGMAX_MARGIN:
+            assert int(eng.argmax.item()) == am
+    assert eng.error() == T.TINFER_OK
+    eng.close()
