@@ -32,6 +32,7 @@ EXPORTS = [
     "tinfer_debug_withhold_results", "tinfer_set_schedule", "tinfer_get_schedule", "tinfer_destroy",
     "tinfer_packed_row_bytes", "tinfer_pack_matrix", "tinfer_op_gemv", "tinfer_op_attention",
     "tinfer_op_attention_noalloc", "tinfer_op_gemv_batch", "tinfer_moe_packed_bytes", "tinfer_pack_moe", "tinfer_op_moe",
+    "tinfer_op_gemm_bf16",
 ]
 
 
@@ -105,6 +106,7 @@ def lib():
             "tinfer_moe_packed_bytes": ([I, I, I, I, I, I], Z),
             "tinfer_pack_moe": ([I, I, I, I, I, I, P, P, P, P, P, P, P, P, P], I),
             "tinfer_op_moe": ([I, I, I, I, I, I, I, P, P, P, P, P, P, P, I, P, P], I),
+            "tinfer_op_gemm_bf16": ([I, I, I, P, P, P, P], I),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -274,6 +276,10 @@ def tinfer_op_moe(fmt, group, scale_dtype, n_experts, top_k, hidden, ffn_e, gu_p
 
 
 # ------------------------------------------------------------------ marshalling helpers
+
+def tinfer_op_gemm_bf16(m, n, k, x, w, y, stream=None) -> int:
+    return lib().tinfer_op_gemm_bf16(m, n, k, _ptr(x), _ptr(w), _ptr(y), _stream(stream))
+
 
 def make_config(c: dict, exec_mode: int = TINFER_MEGAKERNEL) -> tinfer_config:
     """tinfer_config from a workload description (synth.CONFIGS entries or the same keys)."""

@@ -11,7 +11,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libtinfer.so")
-SOURCES = ["mega_bf16.cu", "mega_int4.cu", "kernels.cu", "api.cu"]
+SOURCES = ["mega_bf16.cu", "mega_int4.cu", "kernels.cu", "api.cu", "gemm.cu"]
 HEADERS = ["engine.h", "kernels.h", "ptx.cuh", "step.cuh", "megakernel.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]

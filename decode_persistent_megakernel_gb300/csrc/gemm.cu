@@ -1,0 +1,269 @@
+// gemm.cu -- the dense contraction of a batched prefill on Blackwell's fifth-generation tensor cores:
+// Y[M][N] = X[M][K] W[N][K]^T in bf16 with fp32 accumulation ("How I built an LLM inference engine
+// from scratch in CUDA", "What I'd tell someone starting, and what's next": a prompt processed as
+// one batch makes every linear layer a matrix-matrix product, the case tensor cores are for; and
+// "Llama-1B: optimizing kernels": prefill runs GEMM kernels, decode GEMV kernels). Decode at batch 1
+// stays on the CUDA cores (a matrix-vector stream); this is the path whose M is the prompt length.
+//
+// One CTA computes one 128 x 128 tile of Y. Tensor memory map (TMA) loads bring 128 x 64 tiles of X
+// and W, 128-byte swizzled, into a 4-stage shared-memory ring (full / empty mbarriers); one elected
+// thread issues tcgen05.mma (M = 128, N = 128, K = 16 per instruction, both operands K-major from
+// shared memory, the accumulator in tensor memory) and tcgen05.commit frees a stage once its
+// products are done; four warps then read the accumulator rows out of tensor memory
+// (tcgen05.ld 32x32b) and store them. Every wait is bounded; tensor memory is always released.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "ptx.cuh"
+#include "tinfer.h"
+
+namespace tinfer {
+namespace gemm {
+
+constexpr int BM = 128, BN = 128, BK = 64;  // tile; BK bf16 = 128 bytes, one swizzle atom wide
+constexpr int STAGES = 4;
+constexpr int TILE_BYTES = BM * BK * 2;      // 16 KiB per operand tile
+constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;  // + alignment slack for the 1 KiB atoms
+constexpr int NTHREADS = 128;
+constexpr int EW_GEMM_TIMEOUT = 2;
+
+// Shared-memory matrix descriptor of a K-major operand tile in the 128-byte swizzled layout that a
+// TMA load with CU_TENSOR_MAP_SWIZZLE_128B writes: rows of 128 bytes, groups of 8 rows 1024 bytes
+// apart (stride byte offset), the leading byte offset unused for this layout (1), descriptor
+// version 1, layout type 2 (128-byte swizzle). The tile starts on a 1024-byte boundary.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both K-major, N and M.
+__host__ __device__ constexpr uint32_t instr_desc_bf16(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         int accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// The mbarrier receives one arrival when every tcgen05.mma this thread issued before it is complete.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+
+// Bounded wait for the phase of `parity` of an mbarrier; false when it ran out.
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, long long timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity))
+    if ((long long)(globaltimer() - t0) > timeout_ns) return false;
+  return true;
+}
+
+struct GemmParams {
+  int m, n, k;
+  float* y;       // [m][n] fp32
+  int* err;       // error word (bit EW_GEMM_TIMEOUT: a wait ran out)
+  long long timeout_ns;
+};
+
+__global__ void __launch_bounds__(NTHREADS, 1) gemm_bf16_tcgen05(const __grid_constant__ CUtensorMap map_x,
+                                                                const __grid_constant__ CUtensorMap map_w,
+                                                                const __grid_constant__ GemmParams q) {
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ __align__(8) unsigned long long full[STAGES], empty[STAGES], done;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int bad;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;  // 1 KiB-aligned ring
+  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
+  const int nk = (q.k + BK - 1) / BK;
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_addr(&full[s]), 1);
+      mbar_init(smem_addr(&empty[s]), 1);
+    }
+    mbar_init(smem_addr(&done), 1);
+    bad = 0;
+    mbar_fence_init();
+  }
+  if (warp == 2) {  // tensor memory for the 128 x 128 fp32 accumulator: 128 columns
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&tmem_base_s)),
+                 "r"(BN)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+
+  if (warp == 0 && lane == 0) {
+    // producer: stage s of round r waits until the products of round r - 1 freed it
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % STAGES;
+      const uint32_t r = (uint32_t)(kb / STAGES);
+      if (!bar_wait(smem_addr(&empty[s]), (r & 1u) ^ 1u, q.timeout_ns)) { bad = 1; break; }
+      const uint32_t st = base + (uint32_t)s * STAGE_BYTES;
+      mbar_arrive_expect_tx(smem_addr(&full[s]), STAGE_BYTES);
+      tma_load_2d(st, &map_x, kb * BK, m0, smem_addr(&full[s]));
+      tma_load_2d(st + TILE_BYTES, &map_w, kb * BK, n0, smem_addr(&full[s]));
+    }
+  } else if (warp == 1 && lane == 0) {
+    // MMA issuer: four K = 16 steps per stage, advancing the descriptors 32 bytes inside the atom
+    const uint32_t idesc = instr_desc_bf16(BM, BN);
+    bool ok = true;
+    for (int kb = 0; kb < nk && ok; ++kb) {
+      const int s = kb % STAGES;
+      const uint32_t r = (uint32_t)(kb / STAGES);
+      if (!bar_wait(smem_addr(&full[s]), r & 1u, q.timeout_ns)) { bad = 1; ok = false; break; }
+      tc_fence_after();
+      const uint32_t st = base + (uint32_t)s * STAGE_BYTES;
+#pragma unroll
+      for (int kk = 0; kk < BK / 16; ++kk)
+        mma_bf16(tmem, smem_desc_sw128(st + 32u * kk), smem_desc_sw128(st + TILE_BYTES + 32u * kk), idesc,
+                 (kb | kk) != 0);
+      mma_commit(smem_addr(&empty[s]));  // the stage is free once these products are done
+    }
+    mma_commit(smem_addr(&done));  // the accumulator is complete (or, after a failure, quiet)
+  }
+  __syncwarp();
+
+  // epilogue: warp w reads accumulator rows 32 w .. 32 w + 31 (its quarter of tensor-memory lanes)
+  const bool ready = bar_wait(smem_addr(&done), 0u, q.timeout_ns);
+  tc_fence_after();
+  const int row = m0 + 32 * warp + lane;
+  const bool vec = (q.n & 3) == 0 && (reinterpret_cast<uintptr_t>(q.y) & 15) == 0;
+  for (int c0 = 0; c0 < BN && ready; c0 += 32) {
+    uint32_t v[32];
+    const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)c0;
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+          "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+          "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    if (row < q.m) {
+      float* yr = q.y + (size_t)row * q.n + n0 + c0;
+      const int lim = q.n - (n0 + c0);  // columns of this chunk inside Y
+      if (vec && lim >= 32) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 4)
+          *reinterpret_cast<float4*>(yr + i) = make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                                          __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (i < lim) yr[i] = __uint_as_float(v[i]);
+      }
+    }
+  }
+  if (!ready && tid == 0) bad = 1;
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0 && bad) atomicOr(q.err, EW_GEMM_TIMEOUT);
+  if (warp == 2)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(BN) : "memory");
+}
+
+// ---------------------------------------------------------------------------------------- host
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// A [rows][k] bf16 row-major matrix as a 2-D tensor map with 128 x 64 boxes, 128-byte swizzle and
+// zero fill past its edges.
+bool make_map(CUtensorMap* map, const void* ptr, int rows, int k) {
+  const auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)k * 2};
+  const cuuint32_t box[2] = {BK, BM};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct ErrWord {
+  int* p = nullptr;
+  int device = -1;
+};
+ErrWord g_err;
+std::mutex g_err_mu;
+
+}  // namespace gemm
+}  // namespace tinfer
+
+using namespace tinfer;
+
+extern "C" tinfer_status tinfer_op_gemm_bf16(int m, int n, int k, const void* x_dev, const void* w_dev,
+                                             float* y_dev, void* stream) {
+  if (m <= 0 || n <= 0 || k <= 0 || !x_dev || !w_dev || !y_dev) return TINFER_ERR_INVALID_ARG;
+  // the tensor maps need 16-byte aligned bases and row strides (k a multiple of 8)
+  if (k % 8 || (reinterpret_cast<uintptr_t>(x_dev) & 15) || (reinterpret_cast<uintptr_t>(w_dev) & 15) ||
+      (reinterpret_cast<uintptr_t>(y_dev) & 3))
+    return TINFER_ERR_INVALID_ARG;
+  if ((long long)n > (1LL << 31) / 128 || (long long)m > 65535LL * gemm::BM) return TINFER_ERR_UNSUPPORTED;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return TINFER_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lk(gemm::g_err_mu);
+    if (!gemm::g_err.p || gemm::g_err.device != dev) {
+      if (cudaMalloc(&gemm::g_err.p, 16) != cudaSuccess) return TINFER_ERR_OOM;
+      gemm::g_err.device = dev;
+    }
+  }
+  CUtensorMap mx, mw;
+  if (!gemm::make_map(&mx, x_dev, m, k) || !gemm::make_map(&mw, w_dev, n, k)) return TINFER_ERR_UNSUPPORTED;
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(gemm::gemm_bf16_tcgen05, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    gemm::SMEM_BYTES);
+  });
+  if (attr_err != cudaSuccess) return TINFER_ERR_CUDA;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemsetAsync(gemm::g_err.p, 0, 4, st) != cudaSuccess) return TINFER_ERR_CUDA;
+  gemm::GemmParams q{m, n, k, y_dev, gemm::g_err.p, 200LL * 1000 * 1000};
+  const dim3 grid((n + gemm::BN - 1) / gemm::BN, (m + gemm::BM - 1) / gemm::BM);
+  gemm::gemm_bf16_tcgen05<<<grid, gemm::NTHREADS, gemm::SMEM_BYTES, st>>>(mx, mw, q);
+  if (cudaGetLastError() != cudaSuccess) return TINFER_ERR_CUDA;
+  int h = 0;
+  if (cudaMemcpyAsync(&h, gemm::g_err.p, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess) return TINFER_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return TINFER_ERR_CUDA;
+  return h ? TINFER_ERR_TIMEOUT : TINFER_OK;
+}

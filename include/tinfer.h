@@ -310,6 +310,21 @@ tinfer_status tinfer_op_moe(int weight_format, int group_size, int scale_dtype, 
                             const float* weights_dev, const float* x_dev, float* h_dev, float* y_dev,
                             int accumulate, int32_t* status_dev, void* stream);
 
+/* Dense bf16 matrix product of a batched prefill on the tensor cores ("How I built an LLM inference
+ * engine from scratch in CUDA", "What I'd tell someone starting, and what's next": the prompt's
+ * tokens processed as one batch turn each linear layer's matrix-vector products into one
+ * matrix-matrix product, where tensor cores apply; "Llama-1B: optimizing kernels": GEMM for prefill,
+ * GEMV for decode): y[i][r] = sum_c x[i][c] w[r][c] for i < m, r < n, products of bf16 values
+ * accumulated in fp32 (tcgen05.mma, accumulator in tensor memory).
+ * x_dev: bf16 [m][k] row-major (the prompt's normalised activations), w_dev: bf16 [n][k] row-major
+ * (a canonical weight matrix, or the bf16 rows of a packed layer, which have the same layout),
+ * y_dev: fp32 [m][n] row-major; all caller-owned device memory. k must be a multiple of 8 and x_dev,
+ * w_dev 16-byte aligned (TMA tensor maps), else TINFER_ERR_INVALID_ARG; m and n are free (edges are
+ * zero-filled and masked). Synchronises `stream` before returning; a device wait that ran out
+ * returns TINFER_ERR_TIMEOUT. */
+tinfer_status tinfer_op_gemm_bf16(int m, int n, int k, const void* x_dev, const void* w_dev, float* y_dev,
+                                  void* stream);
+
 /* ---------------------------------------------------------------------------------------------
  * Attention that allocates nothing. The pages have no counterpart of this call: it is an
  * engineering addition for embedders.
