@@ -5,12 +5,14 @@
 // "Llama-1B: optimizing kernels": prefill runs GEMM kernels, decode GEMV kernels). Decode at batch 1
 // stays on the CUDA cores (a matrix-vector stream); this is the path whose M is the prompt length.
 //
-// One CTA computes one 128 x 128 tile of Y. Tensor memory map (TMA) loads bring 128 x 64 tiles of X
-// and W, 128-byte swizzled, into a 4-stage shared-memory ring (full / empty mbarriers); one elected
-// thread issues tcgen05.mma (M = 128, N = 128, K = 16 per instruction, both operands K-major from
-// shared memory, the accumulator in tensor memory) and tcgen05.commit frees a stage once its
-// products are done; four warps then read the accumulator rows out of tensor memory
-// (tcgen05.ld 32x32b) and store them. Every wait is bounded; tensor memory is always released.
+// Persistent CTAs (one per SM) walk 128 x 256 tiles of Y, consecutive CTAs on the same W tile so that
+// it is read from L2 by all of them. Warp 0's elected thread loads 128 x 64 tiles of X and 256 x 64
+// tiles of W with the tensor memory accelerator (TMA), 128-byte swizzled, into a 4-stage
+// shared-memory ring (full / empty mbarriers); warp 1's elected thread issues tcgen05.mma (M 128,
+// N 256, K 16 per instruction, both operands K-major from shared memory) into one of two 256-column
+// accumulators in tensor memory and tcgen05.commit frees each stage when its products are done;
+// warps 4-7 drain the other accumulator (tcgen05.ld 32x32b, each warp its quarter of the lanes)
+// while the next tile is computed. Every wait is bounded; tensor memory is always released.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -24,12 +26,14 @@
 namespace tinfer {
 namespace gemm {
 
-constexpr int BM = 128, BN = 128, BK = 64;  // tile; BK bf16 = 128 bytes, one swizzle atom wide
+constexpr int BM = 128, BN = 256, BK = 64;  // tile; BK bf16 = 128 bytes, one swizzle atom wide
 constexpr int STAGES = 4;
-constexpr int TILE_BYTES = BM * BK * 2;      // 16 KiB per operand tile
-constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+constexpr int A_BYTES = BM * BK * 2;         // 16 KiB of X per stage
+constexpr int B_BYTES = BN * BK * 2;         // 32 KiB of W per stage
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;  // + alignment slack for the 1 KiB atoms
-constexpr int NTHREADS = 128;
+constexpr int NTHREADS = 256;
+constexpr int TMEM_COLS = 2 * BN;            // two fp32 accumulators of 128 lanes x 256 columns
 constexpr int EW_GEMM_TIMEOUT = 2;
 
 // Shared-memory matrix descriptor of a K-major operand tile in the 128-byte swizzled layout that a
@@ -91,25 +95,29 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_bf16_tcgen05(const __grid_co
                                                                 const __grid_constant__ CUtensorMap map_w,
                                                                 const __grid_constant__ GemmParams q) {
   extern __shared__ unsigned char smem_raw[];
-  __shared__ __align__(8) unsigned long long full[STAGES], empty[STAGES], done;
+  __shared__ __align__(8) unsigned long long full[STAGES], empty[STAGES], tfull[2], tempty[2];
   __shared__ uint32_t tmem_base_s;
   __shared__ int bad;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;  // 1 KiB-aligned ring
-  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
+  const int tiles_m = (q.m + BM - 1) / BM, tiles_n = (q.n + BN - 1) / BN;
+  const int ntiles = tiles_m * tiles_n;
   const int nk = (q.k + BK - 1) / BK;
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_addr(&full[s]), 1);
       mbar_init(smem_addr(&empty[s]), 1);
     }
-    mbar_init(smem_addr(&done), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_addr(&tfull[b]), 1);   // the MMA thread's commit
+      mbar_init(smem_addr(&tempty[b]), 4);  // one arrival per epilogue warp
+    }
     bad = 0;
     mbar_fence_init();
   }
-  if (warp == 2) {  // tensor memory for the 128 x 128 fp32 accumulator: 128 columns
+  if (warp == 2) {  // all 512 columns: two 128 x 256 fp32 accumulators
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&tmem_base_s)),
-                 "r"(BN)
+                 "r"(TMEM_COLS)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -117,76 +125,105 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_bf16_tcgen05(const __grid_co
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
+  volatile int* failed = &bad;  // read again on every turn: a failed role stops the others promptly
+  // tile t of this CTA: t = blockIdx.x + i * gridDim.x; consecutive t share the W tile (n)
+  auto tile_mn = [&](int t, int& m0, int& n0) {
+    m0 = (t % tiles_m) * BM;
+    n0 = (t / tiles_m) * BN;
+  };
 
   if (warp == 0 && lane == 0) {
     // producer: stage s of round r waits until the products of round r - 1 freed it
-    for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % STAGES;
-      const uint32_t r = (uint32_t)(kb / STAGES);
-      if (!bar_wait(smem_addr(&empty[s]), (r & 1u) ^ 1u, q.timeout_ns)) { bad = 1; break; }
-      const uint32_t st = base + (uint32_t)s * STAGE_BYTES;
-      mbar_arrive_expect_tx(smem_addr(&full[s]), STAGE_BYTES);
-      tma_load_2d(st, &map_x, kb * BK, m0, smem_addr(&full[s]));
-      tma_load_2d(st + TILE_BYTES, &map_w, kb * BK, n0, smem_addr(&full[s]));
-    }
-  } else if (warp == 1 && lane == 0) {
-    // MMA issuer: four K = 16 steps per stage, advancing the descriptors 32 bytes inside the atom
-    const uint32_t idesc = instr_desc_bf16(BM, BN);
-    bool ok = true;
-    for (int kb = 0; kb < nk && ok; ++kb) {
-      const int s = kb % STAGES;
-      const uint32_t r = (uint32_t)(kb / STAGES);
-      if (!bar_wait(smem_addr(&full[s]), r & 1u, q.timeout_ns)) { bad = 1; ok = false; break; }
-      tc_fence_after();
-      const uint32_t st = base + (uint32_t)s * STAGE_BYTES;
-#pragma unroll
-      for (int kk = 0; kk < BK / 16; ++kk)
-        mma_bf16(tmem, smem_desc_sw128(st + 32u * kk), smem_desc_sw128(st + TILE_BYTES + 32u * kk), idesc,
-                 (kb | kk) != 0);
-      mma_commit(smem_addr(&empty[s]));  // the stage is free once these products are done
-    }
-    mma_commit(smem_addr(&done));  // the accumulator is complete (or, after a failure, quiet)
-  }
-  __syncwarp();
-
-  // epilogue: warp w reads accumulator rows 32 w .. 32 w + 31 (its quarter of tensor-memory lanes)
-  const bool ready = bar_wait(smem_addr(&done), 0u, q.timeout_ns);
-  tc_fence_after();
-  const int row = m0 + 32 * warp + lane;
-  const bool vec = (q.n & 3) == 0 && (reinterpret_cast<uintptr_t>(q.y) & 15) == 0;
-  for (int c0 = 0; c0 < BN && ready; c0 += 32) {
-    uint32_t v[32];
-    const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)c0;
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
-          "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
-          "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-    if (row < q.m) {
-      float* yr = q.y + (size_t)row * q.n + n0 + c0;
-      const int lim = q.n - (n0 + c0);  // columns of this chunk inside Y
-      if (vec && lim >= 32) {
-#pragma unroll
-        for (int i = 0; i < 32; i += 4)
-          *reinterpret_cast<float4*>(yr + i) = make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
-                                                          __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (i < lim) yr[i] = __uint_as_float(v[i]);
+    uint32_t it = 0;
+    for (int t = blockIdx.x; t < ntiles && !*failed; t += gridDim.x) {
+      int m0, n0;
+      tile_mn(t, m0, n0);
+      for (int kb = 0; kb < nk; ++kb, ++it) {
+        const int s = (int)(it % STAGES);
+        const uint32_t r = it / STAGES;
+        if (!bar_wait(smem_addr(&empty[s]), (r & 1u) ^ 1u, q.timeout_ns)) { *failed = 1; break; }
+        const uint32_t st = base + (uint32_t)s * STAGE_BYTES;
+        mbar_arrive_expect_tx(smem_addr(&full[s]), STAGE_BYTES);
+        tma_load_2d(st, &map_x, kb * BK, m0, smem_addr(&full[s]));
+        tma_load_2d(st + A_BYTES, &map_w, kb * BK, n0, smem_addr(&full[s]));
       }
     }
+  } else if (warp == 1 && lane == 0) {
+    // MMA issuer: accumulator b of its u-th use waits until the epilogue drained use u - 1
+    const uint32_t idesc = instr_desc_bf16(BM, BN);
+    uint32_t it = 0, tc = 0;
+    for (int t = blockIdx.x; t < ntiles && !*failed; t += gridDim.x, ++tc) {
+      const uint32_t b = tc & 1u, u = tc >> 1;
+      if (!bar_wait(smem_addr(&tempty[b]), (u & 1u) ^ 1u, q.timeout_ns)) { *failed = 1; break; }
+      tc_fence_after();
+      const uint32_t acc = tmem + b * BN;
+      for (int kb = 0; kb < nk; ++kb, ++it) {
+        const int s = (int)(it % STAGES);
+        const uint32_t r = it / STAGES;
+        if (!bar_wait(smem_addr(&full[s]), r & 1u, q.timeout_ns)) { *failed = 1; break; }
+        tc_fence_after();
+        const uint32_t st = base + (uint32_t)s * STAGE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          mma_bf16(acc, smem_desc_sw128(st + 32u * kk), smem_desc_sw128(st + A_BYTES + 32u * kk), idesc,
+                   (kb | kk) != 0);
+        mma_commit(smem_addr(&empty[s]));  // the stage is free once these products are done
+      }
+      mma_commit(smem_addr(&tfull[b]));  // this tile's accumulator is complete
+      if (*failed) break;
+    }
+  } else if (warp >= 4) {
+    // epilogue: warp 4 + e drains accumulator lanes 32 e .. 32 e + 31 (rows m0 + 32 e + lane)
+    const int e = warp - 4;
+    const bool vec = (q.n & 3) == 0 && (reinterpret_cast<uintptr_t>(q.y) & 15) == 0;
+    uint32_t tc = 0;
+    for (int t = blockIdx.x; t < ntiles && !*failed; t += gridDim.x, ++tc) {
+      const uint32_t b = tc & 1u, u = tc >> 1;
+      if (!bar_wait(smem_addr(&tfull[b]), u & 1u, q.timeout_ns)) { *failed = 1; break; }
+      tc_fence_after();
+      int m0, n0;
+      tile_mn(t, m0, n0);
+      const int row = m0 + 32 * e + lane;
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t v[32];
+        const uint32_t taddr = tmem + ((uint32_t)(32 * e) << 16) + b * BN + (uint32_t)c0;
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+            "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+            : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+              "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+              "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]),
+              "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]),
+              "=r"(v[30]), "=r"(v[31])
+            : "r"(taddr));
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        if (row < q.m) {
+          float* yr = q.y + (size_t)row * q.n + n0 + c0;
+          const int lim = q.n - (n0 + c0);  // columns of this chunk inside Y
+          if (vec && lim >= 32) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+              *reinterpret_cast<float4*>(yr + i) = make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                                              __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i < lim) yr[i] = __uint_as_float(v[i]);
+          }
+        }
+      }
+      // the accumulator may be overwritten once all four warps have read it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&tempty[b]));
+    }
   }
-  if (!ready && tid == 0) bad = 1;
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (tid == 0 && bad) atomicOr(q.err, EW_GEMM_TIMEOUT);
+  if (tid == 0 && *failed) atomicOr(q.err, EW_GEMM_TIMEOUT);
   if (warp == 2)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(BN) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
 }
 
 // ---------------------------------------------------------------------------------------- host
@@ -204,14 +241,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// A [rows][k] bf16 row-major matrix as a 2-D tensor map with 128 x 64 boxes, 128-byte swizzle and
-// zero fill past its edges.
-bool make_map(CUtensorMap* map, const void* ptr, int rows, int k) {
+// A [rows][k] bf16 row-major matrix as a 2-D tensor map with box_rows x 64 boxes, 128-byte swizzle
+// and zero fill past its edges.
+bool make_map(CUtensorMap* map, const void* ptr, int rows, int k, int box_rows) {
   const auto fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)k * 2};
-  const cuuint32_t box[2] = {BK, BM};
+  const cuuint32_t box[2] = {BK, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -237,7 +274,8 @@ extern "C" tinfer_status tinfer_op_gemm_bf16(int m, int n, int k, const void* x_
   if (k % 8 || (reinterpret_cast<uintptr_t>(x_dev) & 15) || (reinterpret_cast<uintptr_t>(w_dev) & 15) ||
       (reinterpret_cast<uintptr_t>(y_dev) & 3))
     return TINFER_ERR_INVALID_ARG;
-  if ((long long)n > (1LL << 31) / 128 || (long long)m > 65535LL * gemm::BM) return TINFER_ERR_UNSUPPORTED;
+  if ((long long)((m + gemm::BM - 1) / gemm::BM) * ((n + gemm::BN - 1) / gemm::BN) > (1LL << 30))
+    return TINFER_ERR_UNSUPPORTED;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return TINFER_ERR_CUDA;
   {
@@ -248,7 +286,8 @@ extern "C" tinfer_status tinfer_op_gemm_bf16(int m, int n, int k, const void* x_
     }
   }
   CUtensorMap mx, mw;
-  if (!gemm::make_map(&mx, x_dev, m, k) || !gemm::make_map(&mw, w_dev, n, k)) return TINFER_ERR_UNSUPPORTED;
+  if (!gemm::make_map(&mx, x_dev, m, k, gemm::BM) || !gemm::make_map(&mw, w_dev, n, k, gemm::BN))
+    return TINFER_ERR_UNSUPPORTED;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
@@ -259,7 +298,10 @@ extern "C" tinfer_status tinfer_op_gemm_bf16(int m, int n, int k, const void* x_
   cudaStream_t st = (cudaStream_t)stream;
   if (cudaMemsetAsync(gemm::g_err.p, 0, 4, st) != cudaSuccess) return TINFER_ERR_CUDA;
   gemm::GemmParams q{m, n, k, y_dev, gemm::g_err.p, 200LL * 1000 * 1000};
-  const dim3 grid((n + gemm::BN - 1) / gemm::BN, (m + gemm::BM - 1) / gemm::BM);
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return TINFER_ERR_CUDA;
+  const long long tiles = (long long)((m + gemm::BM - 1) / gemm::BM) * ((n + gemm::BN - 1) / gemm::BN);
+  const int grid = (int)(tiles < sms ? tiles : sms);  // persistent: one CTA per SM at most
   gemm::gemm_bf16_tcgen05<<<grid, gemm::NTHREADS, gemm::SMEM_BYTES, st>>>(mx, mw, q);
   if (cudaGetLastError() != cudaSuccess) return TINFER_ERR_CUDA;
   int h = 0;

@@ -1,6 +1,7 @@
 """The batched-prefill matrix product on the tensor cores (tinfer_op_gemm_bf16): every output row
 against the oracle's pinned bf16 GEMV of that row, single tiles, several tiles, ragged edges in M, N
-and K, a prefill-shaped QKV product, and rejected arguments."""
+and K, a prefill-shaped QKV product, several tiles per persistent CTA (both tensor-memory
+accumulators reused), and rejected arguments."""
 import numpy as np
 import pytest
 
@@ -57,6 +58,15 @@ def test_gemm_prefill_qkv_shape_sampled_rows():
     m, n, k = 512, 3072, 2048
     X, W, Y = run_gemm(m, n, k, seed=2)
     rows = sorted(set(list(range(0, m, 37)) + [127, 128, 255, 256, 383, 384, 511]))
+    check_rows(X, W, Y, rows)
+
+
+def test_gemm_several_tiles_per_cta_sampled_rows():
+    # 16 x 32 tiles of 128 x 256 on at most one CTA per SM: every CTA computes three or four tiles,
+    # alternating its two tensor-memory accumulators; rows sampled from every tile row
+    m, n, k = 2048, 8192, 256
+    X, W, Y = run_gemm(m, n, k, seed=3)
+    rows = sorted(set(list(range(0, m, 61)) + [127, 128, 1023, 1024, 2047]))
     check_rows(X, W, Y, rows)
 
 
