@@ -46,6 +46,18 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def measured_bf16_tflops():
+    """Dense bf16 peak for a contraction timed alone: MEASURED_PEAKS.json's burst figure, else the
+    earlier single measurement on a GB300."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        if "bf16_tflops" in d:
+            return float(d["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
 KERNEL_SOURCES = ["megakernel.cuh", "step.cuh", "ptx.cuh", "engine.h", "kernels.h", "mega_bf16.cu",
                   "mega_int4.cu"]
 
@@ -286,6 +298,23 @@ def ops_measurements(T, torch, peak):
     out["gemv_batch_bf16_16384x2048"] = res
     del mats
     torch.cuda.empty_cache()
+    # the batched-prefill matrix product on the tensor cores (tinfer_op_gemm_bf16, one call includes
+    # its device-to-host status read): a 2048-token prompt through the Llama-shaped gate/up matrix and
+    # a compute-bound 4096 x 8192 x 8192 product; four weight matrices taken in turn
+    bf16_peak = measured_bf16_tflops()
+    gres = {}
+    for (m, n, k) in ((2048, 16384, 2048), (4096, 8192, 8192)):
+        ws = [torch.from_numpy(synth.normal_bf16(f"bench.gemm.{n}.{k}.{i}", (n, k), 0.0, 0.02, 0).view(np.int16)).cuda()
+              for i in range(4)]
+        xg = torch.from_numpy(synth.normal_bf16(f"bench.gemm.x.{m}.{k}", (m, k), 0.0, 1.0, 0).view(np.int16)).cuda()
+        yg = torch.empty(m, n, device="cuda")
+        ms = timed(lambda i: T.tinfer_op_gemm_bf16(m, n, k, xg, ws[i % 4], yg, st), 16)
+        tf = 2.0 * m * n * k / (ms * 1e-3) / 1e12
+        gres[f"{m}x{n}x{k}"] = {"us_per_call": ms * 1e3, "tflops": tf, "frac": tf / bf16_peak[0],
+                                "peak_kind": bf16_peak[1]}
+        del ws, xg, yg
+        torch.cuda.empty_cache()
+    out["gemm_bf16_tcgen05"] = gres
     return out
 
 
@@ -343,6 +372,8 @@ def main():
                     help="the column-split down projection variant (bf16 workloads, persistent kernel)")
     ap.add_argument("--no-read-probe", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=0, help="steps of the e2e run (default: the workload's)")
+    ap.add_argument("--only-ops", action="store_true",
+                    help="only the op-level measurements (gathered experts, batched GEMV, prefill GEMM)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -356,6 +387,12 @@ def main():
     rank, local, world, dist = dist_setup(args.gpus)
     torch.cuda.set_device(local)
     T.build()
+    if args.only_ops:
+        if rank == 0:
+            print(json.dumps({"ops": ops_measurements(T, torch, measured_peaks()[0])}), flush=True)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
     c = synth.config(args.config, **({"ffn_split": True} if args.ffn_split else {}))
     w = synth.make_model(c, seed=0)
     P = c["prefill"] + c["prompt"]
