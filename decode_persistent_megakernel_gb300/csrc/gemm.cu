@@ -5,8 +5,9 @@
 // "Llama-1B: optimizing kernels": prefill runs GEMM kernels, decode GEMV kernels). Decode at batch 1
 // stays on the CUDA cores (a matrix-vector stream); this is the path whose M is the prompt length.
 //
-// Persistent CTAs (one per SM) walk 128 x 256 tiles of Y, consecutive CTAs on the same W tile so that
-// it is read from L2 by all of them. Warp 0's elected thread loads 128 x 64 tiles of X and 256 x 64
+// Persistent CTAs (one per SM) walk 128 x 256 tiles of Y (128 x 128 when the wider tiles would not
+// cover the SMs: a short prompt), consecutive CTAs on the same W tile so that it is read from L2 by
+// all of them. Warp 0's elected thread loads 128 x 64 tiles of X and 256 x 64
 // tiles of W with the tensor memory accelerator (TMA), 128-byte swizzled, into a 4-stage
 // shared-memory ring (full / empty mbarriers); warp 1's elected thread issues tcgen05.mma (M 128,
 // N 256, K 16 per instruction, both operands K-major from shared memory) into one of two 256-column
@@ -26,14 +27,20 @@
 namespace tinfer {
 namespace gemm {
 
-constexpr int BM = 128, BN = 256, BK = 64;  // tile; BK bf16 = 128 bytes, one swizzle atom wide
-constexpr int STAGES = 4;
+constexpr int BM = 128, BK = 64;             // tile rows; BK bf16 = 128 bytes, one swizzle atom wide
 constexpr int A_BYTES = BM * BK * 2;         // 16 KiB of X per stage
-constexpr int B_BYTES = BN * BK * 2;         // 32 KiB of W per stage
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;  // + alignment slack for the 1 KiB atoms
 constexpr int NTHREADS = 256;
-constexpr int TMEM_COLS = 2 * BN;            // two fp32 accumulators of 128 lanes x 256 columns
+// Tile width BN (256, or 128 when 256-wide tiles would leave SMs idle): W bytes per stage, stages
+// (the ring holds about 192 KiB), the dynamic shared memory with 1 KiB of alignment slack, and two
+// fp32 accumulators of 128 lanes x BN columns in tensor memory.
+template <int BN>
+struct Tile {
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+  static constexpr int TMEM_COLS = 2 * BN;
+};
 constexpr int EW_GEMM_TIMEOUT = 2;
 
 // Shared-memory matrix descriptor of a K-major operand tile in the 128-byte swizzled layout that a
@@ -91,13 +98,16 @@ struct GemmParams {
   long long timeout_ns;
 };
 
+template <int BN>
 __global__ void __launch_bounds__(NTHREADS, 1) gemm_bf16_tcgen05(const __grid_constant__ CUtensorMap map_x,
                                                                 const __grid_constant__ CUtensorMap map_w,
                                                                 const __grid_constant__ GemmParams q) {
+  constexpr int STAGES = Tile<BN>::STAGES, STAGE_BYTES = Tile<BN>::STAGE_BYTES, TMEM_COLS = Tile<BN>::TMEM_COLS;
   extern __shared__ unsigned char smem_raw[];
   __shared__ __align__(8) unsigned long long full[STAGES], empty[STAGES], tfull[2], tempty[2];
   __shared__ uint32_t tmem_base_s;
   __shared__ int bad;
+  __shared__ int go[2];  // epilogue: the poller's decision for tiles of even and odd parity
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;  // 1 KiB-aligned ring
   const int tiles_m = (q.m + BM - 1) / BM, tiles_n = (q.n + BN - 1) / BN;
@@ -115,7 +125,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_bf16_tcgen05(const __grid_co
     bad = 0;
     mbar_fence_init();
   }
-  if (warp == 2) {  // all 512 columns: two 128 x 256 fp32 accumulators
+  if (warp == 2) {  // two 128 x BN fp32 accumulators
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&tmem_base_s)),
                  "r"(TMEM_COLS)
                  : "memory");
@@ -177,9 +187,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_bf16_tcgen05(const __grid_co
     const int e = warp - 4;
     const bool vec = (q.n & 3) == 0 && (reinterpret_cast<uintptr_t>(q.y) & 15) == 0;
     uint32_t tc = 0;
-    for (int t = blockIdx.x; t < ntiles && !*failed; t += gridDim.x, ++tc) {
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tc) {
       const uint32_t b = tc & 1u, u = tc >> 1;
-      if (!bar_wait(smem_addr(&tfull[b]), u & 1u, q.timeout_ns)) { *failed = 1; break; }
+      // one thread polls for the accumulator; the other epilogue threads wait at a named barrier,
+      // which takes no issue slots from the producer and MMA threads sharing their schedulers. The
+      // poller's decision (in a slot of its own per tile parity) is what every epilogue thread
+      // follows, so that all of them pass the same barriers.
+      if (e == 0 && lane == 0) {
+        const bool ok = !*failed && bar_wait(smem_addr(&tfull[b]), u & 1u, q.timeout_ns);
+        if (!ok) *failed = 1;
+        go[tc & 1u] = ok ? 1 : 0;
+      }
+      named_sync(1, 128);
+      if (!reinterpret_cast<volatile int*>(go)[tc & 1u]) break;
       tc_fence_after();
       int m0, n0;
       tile_mn(t, m0, n0);
@@ -274,8 +294,7 @@ extern "C" tinfer_status tinfer_op_gemm_bf16(int m, int n, int k, const void* x_
   if (k % 8 || (reinterpret_cast<uintptr_t>(x_dev) & 15) || (reinterpret_cast<uintptr_t>(w_dev) & 15) ||
       (reinterpret_cast<uintptr_t>(y_dev) & 3))
     return TINFER_ERR_INVALID_ARG;
-  if ((long long)((m + gemm::BM - 1) / gemm::BM) * ((n + gemm::BN - 1) / gemm::BN) > (1LL << 30))
-    return TINFER_ERR_UNSUPPORTED;
+  if ((long long)((m + gemm::BM - 1) / gemm::BM) * ((n + 127) / 128) > (1LL << 30)) return TINFER_ERR_UNSUPPORTED;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return TINFER_ERR_CUDA;
   {
@@ -285,24 +304,33 @@ extern "C" tinfer_status tinfer_op_gemm_bf16(int m, int n, int k, const void* x_
       gemm::g_err.device = dev;
     }
   }
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return TINFER_ERR_CUDA;
+  // 128 x 256 tiles, or 128 x 128 ones when the wider tiles would not cover the SMs (short prompts)
+  const long long tiles_m = (m + gemm::BM - 1) / gemm::BM;
+  const int bn = tiles_m * ((n + 255) / 256) < sms ? 128 : 256;
+  const long long tiles = tiles_m * ((n + bn - 1) / bn);
   CUtensorMap mx, mw;
-  if (!gemm::make_map(&mx, x_dev, m, k, gemm::BM) || !gemm::make_map(&mw, w_dev, n, k, gemm::BN))
+  if (!gemm::make_map(&mx, x_dev, m, k, gemm::BM) || !gemm::make_map(&mw, w_dev, n, k, bn))
     return TINFER_ERR_UNSUPPORTED;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(gemm::gemm_bf16_tcgen05, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    gemm::SMEM_BYTES);
+    attr_err = cudaFuncSetAttribute(gemm::gemm_bf16_tcgen05<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    gemm::Tile<256>::SMEM_BYTES);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(gemm::gemm_bf16_tcgen05<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      gemm::Tile<128>::SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return TINFER_ERR_CUDA;
   cudaStream_t st = (cudaStream_t)stream;
   if (cudaMemsetAsync(gemm::g_err.p, 0, 4, st) != cudaSuccess) return TINFER_ERR_CUDA;
   gemm::GemmParams q{m, n, k, y_dev, gemm::g_err.p, 200LL * 1000 * 1000};
-  int sms = 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return TINFER_ERR_CUDA;
-  const long long tiles = (long long)((m + gemm::BM - 1) / gemm::BM) * ((n + gemm::BN - 1) / gemm::BN);
   const int grid = (int)(tiles < sms ? tiles : sms);  // persistent: one CTA per SM at most
-  gemm::gemm_bf16_tcgen05<<<grid, gemm::NTHREADS, gemm::SMEM_BYTES, st>>>(mx, mw, q);
+  if (bn == 256)
+    gemm::gemm_bf16_tcgen05<256><<<grid, gemm::NTHREADS, gemm::Tile<256>::SMEM_BYTES, st>>>(mx, mw, q);
+  else
+    gemm::gemm_bf16_tcgen05<128><<<grid, gemm::NTHREADS, gemm::Tile<128>::SMEM_BYTES, st>>>(mx, mw, q);
   if (cudaGetLastError() != cudaSuccess) return TINFER_ERR_CUDA;
   int h = 0;
   if (cudaMemcpyAsync(&h, gemm::g_err.p, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess) return TINFER_ERR_CUDA;
