@@ -1296,11 +1296,13 @@ static __device__ void attn_merge(const AttnArgs& A, Misc* ms, int tid, int j, i
 // 32 / LG consecutive rows: no bank conflicts). The GP partial sums then meet by a reduce-scatter
 // over the group (each level halves the values a lane keeps), which leaves head li / (LG / GP) in
 // lane li after log2(GP) + log2(LG / GP) shuffles per position instead of GP * log2(LG).
+// A warp takes two positions per lane group and loop turn, with no branch between them, so that the
+// two dependent chains (key load, dot products, shuffles) overlap: the step is latency-bound.
 template <int GP, int LG>
 __device__ __forceinline__ void attn_scores_groups(uint32_t kst, const float* qs, const float* kn,
                                                    float* sc, int nk, int T, int G, int tid) {
   static_assert(GP <= LG, "a lane keeps at least one head");
-  constexpr int D = LG * 8, PW = 32 / LG, NW = NCT / 32;
+  constexpr int D = LG * 8, PW = 32 / LG, NW = NCT / 32, STEP = NW * PW;
   const int lane = tid & 31, warp = tid >> 5;
   const int li = lane % LG, pl = lane / LG;
   float qr[GP][8];
@@ -1312,19 +1314,25 @@ __device__ __forceinline__ void attn_scores_groups(uint32_t kst, const float* qs
     qr[g][0] = on ? a.x : 0.f; qr[g][1] = on ? a.y : 0.f; qr[g][2] = on ? a.z : 0.f; qr[g][3] = on ? a.w : 0.f;
     qr[g][4] = on ? b.x : 0.f; qr[g][5] = on ? b.y : 0.f; qr[g][6] = on ? b.z : 0.f; qr[g][7] = on ? b.w : 0.f;
   }
+  // the new position's key chunk (read only where t == nk; stale but unused in a chunk without pos)
+  float kn8[8];
+  {
+    const float4 a = *reinterpret_cast<const float4*>(kn + li * 8);
+    const float4 b = *reinterpret_cast<const float4*>(kn + li * 8 + 4);
+    kn8[0] = a.x; kn8[1] = a.y; kn8[2] = a.z; kn8[3] = a.w; kn8[4] = b.x; kn8[5] = b.y; kn8[6] = b.z; kn8[7] = b.w;
+  }
   const uint4* Ks = sptr<uint4>(kst);
-  for (int tb = warp * PW; tb < T; tb += NW * PW) {
-    const int t = tb + pl;
-    float k8[8];
-    if (t < nk) {
-      const uint4 kv = Ks[(size_t)t * LG + li];
-      k8[0] = bf16_lo(kv.x); k8[1] = bf16_hi(kv.x); k8[2] = bf16_lo(kv.y); k8[3] = bf16_hi(kv.y);
-      k8[4] = bf16_lo(kv.z); k8[5] = bf16_hi(kv.z); k8[6] = bf16_lo(kv.w); k8[7] = bf16_hi(kv.w);
-    } else {  // the new position (t == nk) or past the chunk (t >= T: result unused)
+  const int kl = nk > 0 ? nk - 1 : 0;  // rows past the cached ones read row kl: always in the stage
+  // key chunk of position t: cached row, the new key, or zeros past the chunk (result unused)
+  auto key = [&](int t, float (&k8)[8]) {
+    const uint4 kv = Ks[(size_t)min(t, kl) * LG + li];
+    const float c[8] = {bf16_lo(kv.x), bf16_hi(kv.x), bf16_lo(kv.y), bf16_hi(kv.y),
+                        bf16_lo(kv.z), bf16_hi(kv.z), bf16_lo(kv.w), bf16_hi(kv.w)};
+    const bool cached = t < nk, fresh = t < T;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) k8[e] = t < T ? kn[li * 8 + e] : 0.f;
-    }
-    float v[GP];
+    for (int e = 0; e < 8; ++e) k8[e] = cached ? c[e] : fresh ? kn8[e] : 0.f;
+  };
+  auto dots = [&](const float (&k8)[8], float (&v)[GP]) {
 #pragma unroll
     for (int g = 0; g < GP; ++g) {
       float a = 0.f;
@@ -1332,7 +1340,9 @@ __device__ __forceinline__ void attn_scores_groups(uint32_t kst, const float* qs
       for (int e = 0; e < 8; ++e) a = fmaf(qr[g][e], k8[e], a);
       v[g] = a;
     }
-    // reduce-scatter over the LG lanes of the group
+  };
+  // reduce-scatter over the LG lanes of the group
+  auto reduce = [&](float (&v)[GP]) {
 #pragma unroll
     for (int n = GP, off = LG / 2; off > 0; off >>= 1) {
       const bool up = (li & off) != 0;
@@ -1350,8 +1360,20 @@ __device__ __forceinline__ void attn_scores_groups(uint32_t kst, const float* qs
         v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
       }
     }
-    const int head = li / (LG / GP);
-    if (li % (LG / GP) == 0 && head < G && t < T) sc[head * T_MAX + t] = v[0];
+  };
+  const int head = li / (LG / GP);
+  const bool writer = li % (LG / GP) == 0 && head < G;
+  for (int tb = warp * PW; tb < T; tb += 2 * STEP) {
+    const int ta = tb + pl, tc = tb + STEP + pl;
+    float ka[8], kc[8], va[GP], vc[GP];
+    key(ta, ka);
+    key(tc, kc);
+    dots(ka, va);
+    dots(kc, vc);
+    reduce(va);
+    reduce(vc);
+    if (writer && ta < T) sc[head * T_MAX + ta] = va[0];
+    if (writer && tc < T) sc[head * T_MAX + tc] = vc[0];
   }
 }
 
@@ -1402,7 +1424,7 @@ __device__ __forceinline__ void attn_scores_threads(uint32_t kst, const float* q
 // with head j merges. The work is spread so that no step waits on a long dependent chain:
 //   scores: one thread per (head, position), a full dot product over d; the 16-byte key chunks are
 //           visited in a rotated order so that the 8 lanes of a quarter-warp hit distinct banks;
-//   values: one thread per (head, dimension), four independent accumulators over the positions.
+//   values: one thread per (head, dimension pair), eight positions per turn into four accumulators.
 // tr: optional timeline row of the phase (fields TR_READY, TR_ACT, TR_ENTRY, TR_AUX0, TR_FETCHED,
 // TR_AUX1 receive the keys' arrival, the ends of the query set-up and the scores, the values'
 // arrival, the end of the partials and the merge start).
@@ -1515,14 +1537,27 @@ static __device__ bool attn_unit(Pipe& pp, const AttnArgs& A, const AttnSplit& s
   named_sync(BAR_CONS, NCT);
   if (tr && tid == 0) tr[TR_ENTRY] = globaltimer();
 
-  // ---- softmax statistics per head (unnormalised probabilities stay in sc)
+  // ---- softmax statistics per head (unnormalised probabilities stay in sc); a lane's first two
+  // scores stay in registers between the maximum and the exponentials, the rest (T > 64) is re-read
   if (warp < G) {
     float* sg = sc + warp * T_MAX;
-    float m = -CUDART_INF_F;
-    for (int t = lane; t < T; t += 32) m = fmaxf(m, sg[t]);
+    const float s0 = lane < T ? sg[lane] : -CUDART_INF_F;
+    const float s1 = lane + 32 < T ? sg[lane + 32] : -CUDART_INF_F;
+    float m = fmaxf(s0, s1);
+    for (int t = lane + 64; t < T; t += 32) m = fmaxf(m, sg[t]);
     m = warp_max(m);
     float l = 0.f;
-    for (int t = lane; t < T; t += 32) {
+    if (lane < T) {
+      const float e = expf(s0 - m);
+      sg[lane] = e;
+      l += e;
+    }
+    if (lane + 32 < T) {
+      const float e = expf(s1 - m);
+      sg[lane + 32] = e;
+      l += e;
+    }
+    for (int t = lane + 64; t < T; t += 32) {
       const float e = expf(sg[t] - m);
       sg[t] = e;
       l += e;
@@ -1543,6 +1578,23 @@ static __device__ bool attn_unit(Pipe& pp, const AttnArgs& A, const AttnSplit& s
       const uint32_t* vc = Vw + i2;
       float2 o0 = make_float2(0.f, 0.f), o1 = o0, o2 = o0, o3 = o0;
       int t = 0;
+      // eight positions per turn, position t always into accumulator t mod 4 in order: the loads
+      // of a turn issue together (the step is latency-bound), the sums are those of the 4-wide loop
+      for (; t + 8 <= nk; t += 8) {
+        const float4 pa = *reinterpret_cast<const float4*>(pg + t);
+        const float4 pb = *reinterpret_cast<const float4*>(pg + t + 4);
+        uint32_t w[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) w[u] = vc[(size_t)(t + u) * half];
+        o0 = fma2(make_float2(pa.x, pa.x), make_float2(bf16_lo(w[0]), bf16_hi(w[0])), o0);
+        o1 = fma2(make_float2(pa.y, pa.y), make_float2(bf16_lo(w[1]), bf16_hi(w[1])), o1);
+        o2 = fma2(make_float2(pa.z, pa.z), make_float2(bf16_lo(w[2]), bf16_hi(w[2])), o2);
+        o3 = fma2(make_float2(pa.w, pa.w), make_float2(bf16_lo(w[3]), bf16_hi(w[3])), o3);
+        o0 = fma2(make_float2(pb.x, pb.x), make_float2(bf16_lo(w[4]), bf16_hi(w[4])), o0);
+        o1 = fma2(make_float2(pb.y, pb.y), make_float2(bf16_lo(w[5]), bf16_hi(w[5])), o1);
+        o2 = fma2(make_float2(pb.z, pb.z), make_float2(bf16_lo(w[6]), bf16_hi(w[6])), o2);
+        o3 = fma2(make_float2(pb.w, pb.w), make_float2(bf16_lo(w[7]), bf16_hi(w[7])), o3);
+      }
       for (; t + 4 <= nk; t += 4) {
         const float4 p4 = *reinterpret_cast<const float4*>(pg + t);
         const uint32_t w0 = vc[(size_t)t * half], w1 = vc[(size_t)(t + 1) * half];
