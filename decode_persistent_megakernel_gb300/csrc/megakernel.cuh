@@ -31,6 +31,8 @@ __device__ __forceinline__ GemvDesc phase_gemv(const StepParams& p, int phase, i
   g.group = m.group;
   g.scale_bf16 = m.scale_bf16;
   g.quantum = 1;
+  g.nsegs = 0;
+  g.rbs = 0;
   const LayerDev& L = p.layers[layer];
   switch (phase) {
     case PH_QKV: g.w = L.qkv; g.rows = m.qkv_rows; g.cols = m.H; g.rb = m.rb_h; break;

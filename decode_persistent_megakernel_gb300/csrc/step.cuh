@@ -399,7 +399,9 @@ struct GemvDesc {
   int quantum;  // 2: rows come in (gate, up) pairs that one stage never splits
   // segment-major stages (gemv_rows<..., SEGMAJOR>): a stage holds nsegs blocks, block s the stage's
   // rows of segment s (rbs bytes per row), as gathered from nsegs separate matrices
-  int nsegs = 0, rbs = 0;
+  // (both 0 for row-major stages; no default member initialisers, so that a __shared__ table of
+  // descriptors needs no constructor)
+  int nsegs, rbs;
 };
 
 // Rows of a matrix owned by one CTA: an even split of row quanta; nr rows per ring stage.
