@@ -309,8 +309,7 @@ __device__ __forceinline__ void produce_step(const StepParams& p, Pipe& pp, unsi
 
 // Consumer side of one attention phase (every unit this CTA owns). Separate from the GEMV phase so
 // that each gets its own register allocation; the pipe state goes in and comes back by value.
-// PAIRED: two key positions per loop turn in the scores (attn_scores_groups).
-template <bool LOOP, bool PAIRED = true>
+template <bool LOOP>
 __device__ __forceinline__ bool consume_attn_phase(const StepParams& p, Pipe& pp, int layer, int pos,
                                                    int tid, int k, unsigned long long* trace, unsigned ep) {
   unsigned long long* tr_ready = trace_at(trace, p, k, TR_READY);
@@ -322,7 +321,7 @@ __device__ __forceinline__ bool consume_attn_phase(const StepParams& p, Pipe& pp
   const int units = A.nkv * sp.nch;
   unsigned long long* tr = trace_at(trace, p, k, 0);  // the first unit of the CTA records sub-steps
   for (int u = blockIdx.x; u < units; u += p.grid) {
-    if (!attn_unit<PAIRED>(pp, A, sp, u / sp.nch, u % sp.nch, tid, tr)) return false;
+    if (!attn_unit(pp, A, sp, u / sp.nch, u % sp.nch, tid, tr)) return false;
     tr = nullptr;
   }
   if (A.pmw) {  // every unit of the CTA has published its partials: now merge the slices
@@ -545,12 +544,12 @@ __device__ __forceinline__ GemvPlan plan_phase(const StepParams& p, Pipe& pp, in
   return plan_gemv(p, pp, phase, layer, k, token, tid, tab, ep);
 }
 
-template <int FMT, int NCHL, int IF, bool LOOP, bool SPLIT, bool PAIRED = true>
+template <int FMT, int NCHL, int IF, bool LOOP, bool SPLIT>
 __device__ __forceinline__ bool run_phase(const StepParams& p, Pipe& pp, const GemvPlan& pl, int k,
                                           int pos, int tid, unsigned long long* trace, unsigned ep) {
   int phase, layer;
   phase_of(k, p.m.L, phase, layer);
-  if (phase == PH_ATTN) return consume_attn_phase<LOOP, PAIRED>(p, pp, layer, pos, tid, k, trace, ep);
+  if (phase == PH_ATTN) return consume_attn_phase<LOOP>(p, pp, layer, pos, tid, k, trace, ep);
   return run_gemv_phase<FMT, NCHL, IF, LOOP, SPLIT>(p, pp, pl, phase, tid, k, trace);
 }
 
@@ -720,9 +719,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) decode_phase_kernel(const __grid_
       const int token = p.step_dev[0], pos = p.step_dev[1];
       // after the wait: reads x of the previous kernel
       const GemvPlan plan = plan_phase(p, pp, k, token, tid, nullptr, p.epoch);
-      // the int4 instances score one key position per turn: at 96 registers the paired scores spill
-      // (the int4 graph step 1.53 -> 1.60 ms), while the bf16 instances gain from them
-      (void)run_phase<FMT, NCHL, 4, false, false, FMT == 0>(p, pp, plan, k, pos, tid, p.trace, p.epoch);
+      (void)run_phase<FMT, NCHL, 4, false, false>(p, pp, plan, k, pos, tid, p.trace, p.epoch);
     }
     named_sync(BAR_CONS, NCT);
     if (tid == 0) *reinterpret_cast<volatile int*>(&pp.ms->cons_done) = 1;

@@ -1298,11 +1298,9 @@ static __device__ void attn_merge(const AttnArgs& A, Misc* ms, int tid, int j, i
 // 32 / LG consecutive rows: no bank conflicts). The GP partial sums then meet by a reduce-scatter
 // over the group (each level halves the values a lane keeps), which leaves head li / (LG / GP) in
 // lane li after log2(GP) + log2(LG / GP) shuffles per position instead of GP * log2(LG).
-// PAIRED: a warp takes two positions per lane group and loop turn, with no branch between them, so
-// that the two dependent chains (key load, dot products, shuffles) overlap (the step is latency-
-// bound); otherwise one (fewer registers: the per-phase int4 kernels, held to 96, spill less). Each
-// score is the same arithmetic either way.
-template <int GP, int LG, bool PAIRED>
+// A warp takes two positions per lane group and loop turn, with no branch between them, so that the
+// two dependent chains (key load, dot products, shuffles) overlap: the step is latency-bound.
+template <int GP, int LG>
 __device__ __forceinline__ void attn_scores_groups(uint32_t kst, const float* qs, const float* kn,
                                                    float* sc, int nk, int T, int G, int tid) {
   static_assert(GP <= LG, "a lane keeps at least one head");
@@ -1367,28 +1365,17 @@ __device__ __forceinline__ void attn_scores_groups(uint32_t kst, const float* qs
   };
   const int head = li / (LG / GP);
   const bool writer = li % (LG / GP) == 0 && head < G;
-  if constexpr (PAIRED) {
-    for (int tb = warp * PW; tb < T; tb += 2 * STEP) {
-      const int ta = tb + pl, tc = tb + STEP + pl;
-      float ka[8], kc[8], va[GP], vc[GP];
-      key(ta, ka);
-      key(tc, kc);
-      dots(ka, va);
-      dots(kc, vc);
-      reduce(va);
-      reduce(vc);
-      if (writer && ta < T) sc[head * T_MAX + ta] = va[0];
-      if (writer && tc < T) sc[head * T_MAX + tc] = vc[0];
-    }
-  } else {
-    for (int tb = warp * PW; tb < T; tb += STEP) {
-      const int ta = tb + pl;
-      float ka[8], va[GP];
-      key(ta, ka);
-      dots(ka, va);
-      reduce(va);
-      if (writer && ta < T) sc[head * T_MAX + ta] = va[0];
-    }
+  for (int tb = warp * PW; tb < T; tb += 2 * STEP) {
+    const int ta = tb + pl, tc = tb + STEP + pl;
+    float ka[8], kc[8], va[GP], vc[GP];
+    key(ta, ka);
+    key(tc, kc);
+    dots(ka, va);
+    dots(kc, vc);
+    reduce(va);
+    reduce(vc);
+    if (writer && ta < T) sc[head * T_MAX + ta] = va[0];
+    if (writer && tc < T) sc[head * T_MAX + tc] = vc[0];
   }
 }
 
@@ -1443,7 +1430,6 @@ __device__ __forceinline__ void attn_scores_threads(uint32_t kst, const float* q
 // tr: optional timeline row of the phase (fields TR_READY, TR_ACT, TR_ENTRY, TR_AUX0, TR_FETCHED,
 // TR_AUX1 receive the keys' arrival, the ends of the query set-up and the scores, the values'
 // arrival, the end of the partials and the merge start).
-template <bool PAIRED = true>
 static __device__ bool attn_unit(Pipe& pp, const AttnArgs& A, const AttnSplit& sp, int j, int c, int tid,
                                  unsigned long long* tr = nullptr) {
   Misc* ms = pp.ms;
@@ -1544,10 +1530,10 @@ static __device__ bool attn_unit(Pipe& pp, const AttnArgs& A, const AttnSplit& s
   // ---- scores
   const uint32_t kst = cons_acquire(pp);
   if (tr && tid == 0) tr[TR_READY] = globaltimer();  // the chunk's keys have arrived
-  if (d == 64 && G <= 4) attn_scores_groups<4, 8, PAIRED>(kst, qs, kn, sc, nk, T, G, tid);
-  else if (d == 64) attn_scores_groups<8, 8, PAIRED>(kst, qs, kn, sc, nk, T, G, tid);
-  else if (d == 128 && G <= 4) attn_scores_groups<4, 16, PAIRED>(kst, qs, kn, sc, nk, T, G, tid);
-  else if (d == 128) attn_scores_groups<8, 16, PAIRED>(kst, qs, kn, sc, nk, T, G, tid);
+  if (d == 64 && G <= 4) attn_scores_groups<4, 8>(kst, qs, kn, sc, nk, T, G, tid);
+  else if (d == 64) attn_scores_groups<8, 8>(kst, qs, kn, sc, nk, T, G, tid);
+  else if (d == 128 && G <= 4) attn_scores_groups<4, 16>(kst, qs, kn, sc, nk, T, G, tid);
+  else if (d == 128) attn_scores_groups<8, 16>(kst, qs, kn, sc, nk, T, G, tid);
   else attn_scores_threads(kst, qs, kn, sc, nk, T, G, d, tid);
   cons_release(pp, lane);
   named_sync(BAR_CONS, NCT);
