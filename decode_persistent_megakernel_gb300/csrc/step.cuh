@@ -1422,10 +1422,13 @@ __device__ __forceinline__ void attn_scores_threads(uint32_t kst, const float* q
 // pos, on the new key, which is written to the cache with the new value), scores over the chunk,
 // per-head max / exponentials / sum, the value sum, and the partial (m, l, o) of the chunk
 // ("One launch per token", "The attention trap"; "How I built an LLM inference engine", "Round 2":
-// one unit per KV head and chunk serving all grouped query heads, K/V read once). The last CTA done
-// with head j merges. The work is spread so that no step waits on a long dependent chain:
-//   scores: one thread per (head, position), a full dot product over d; the 16-byte key chunks are
-//           visited in a rotated order so that the 8 lanes of a quarter-warp hit distinct banks;
+// one unit per KV head and chunk serving all grouped query heads, K/V read once). With plain
+// partials (per-phase kernels) the last CTA done with head j merges; with stamped partials (the
+// persistent kernel) every unit later merges a slice of its head (attn_merge_slice). The work is
+// spread so that no step waits on a long dependent chain:
+//   scores: d / 8 lanes per position holding the group's heads, two positions per turn
+//           (attn_scores_groups); other head sizes one thread per (head, position);
+//   softmax: one warp per head, its first 64 scores kept in registers;
 //   values: one thread per (head, dimension pair), eight positions per turn into four accumulators.
 // tr: optional timeline row of the phase (fields TR_READY, TR_ACT, TR_ENTRY, TR_AUX0, TR_FETCHED,
 // TR_AUX1 receive the keys' arrival, the ends of the query set-up and the scores, the values'
