@@ -97,6 +97,21 @@ def measured_traffic(kernel: str, workload: str):
     return int(kv["dram_bytes_per_launch"])
 
 
+BLOCK_STEPS = 64  # steps per block of the per-step time distribution
+
+
+def block_stats(marks: list) -> dict | None:
+    """Per-step time over blocks of the timed region: marks = [(step index, ms since the region's
+    start)] at the block boundaries, first (0, 0) and last (steps, total). Returns the median, 10th
+    and 90th percentile (linear interpolation) of the blocks' ms per step, or None for one block."""
+    per = [(t1 - t0) / (i1 - i0) for (i0, t0), (i1, t1) in zip(marks, marks[1:]) if i1 > i0]
+    if len(per) < 2:
+        return None
+    q = np.percentile(np.array(per), [10, 50, 90])
+    return {"block_steps": BLOCK_STEPS, "blocks": len(per), "median": float(q[1]), "p10": float(q[0]),
+            "p90": float(q[2])}
+
+
 def algorithmic_bytes(c: dict, pos: int) -> int:
     """Bytes one step must move at position pos: every weight once in its stored format (linears,
     norms, biases, int4 scales), the LM head once, one embedding row, the K/V cache read over
@@ -427,19 +442,26 @@ def main():
         steps = int(max_over_ranks(dist, torch, float(steps)))
         toks = torch.zeros(steps + 1, dtype=torch.int32, device="cuda")
         toks[0] = first
+        # block boundaries for the per-step time distribution (events made before the region)
+        bev = {i: torch.cuda.Event(enable_timing=True) for i in range(BLOCK_STEPS, steps, BLOCK_STEPS)}
         barrier(dist, torch)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with ClockSampler(local) as clk:
             barrier(dist, torch)
             e0.record(st)
             for i in range(steps):
+                if i in bev:
+                    bev[i].record(st)
                 eng.step_dev(toks[i:i + 1], P + (i % S), stream=st, logits=False, argmax=toks[i + 1:i + 2])
             e1.record(st)
             barrier(dist, torch)
         ms = e0.elapsed_time(e1)
+        dist_ms = block_stats([(0, 0.0)] + [(i, e0.elapsed_time(ev)) for i, ev in sorted(bev.items())] +
+                              [(steps, ms)])
         assert eng.error() == T.TINFER_OK
         ms_max = max_over_ranks(dist, torch, ms)
         results[name] = dict(ms_total=ms_max, ms_step=ms_max / steps, steps=steps, clocks=clk.summary(),
+                             dist=dist_ms,
                              launches=steps * eng.query(T.TINFER_Q_KERNELS_PER_STEP),
                              grid=eng.query(T.TINFER_Q_GRID), smem=eng.query(T.TINFER_Q_SMEM),
                              threads=eng.query(T.TINFER_Q_BLOCK_THREADS),
@@ -537,6 +559,7 @@ def main():
         "steps_requested": args.steps,
         "warmup": args.warmup,
         "ms_per_step": r["ms_step"],
+        "ms_per_step_blocks": r["dist"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -555,6 +578,7 @@ def main():
                      "kernel": "decode_megakernel" if main_mode == "mega" else "whole graph",
                      "peak_kind": peak_kind},
         "read_probe_gbs": read_gbs,
+        "floor_frac_read_probe": achieved / read_gbs if read_gbs else None,
         "cpu_baseline": cpu,
         "e2e": {"value": results["e2e"]["value"], "unit": "tokens/s", "h2d_bytes_per_step": 4,
                 "d2h_bytes_per_step": 4},

@@ -1,7 +1,8 @@
 """Host-side pieces of bench.py that the reported numbers rest on (no GPU): the algorithmic bytes of
 one step (the roofline numerator), written out here from the matrix shapes of the
 Llama-3.2-1B-shaped workload; the kernel-source hash that keeps a recorded ncu traffic figure tied
-to the code it was measured on; and the lookup of that figure."""
+to the code it was measured on; the lookup of that figure; the per-step time distribution over
+blocks of the timed region."""
 import os
 import shutil
 
@@ -51,3 +52,16 @@ def test_measured_traffic_only_while_the_sources_match(tmp_path, monkeypatch):
     f.write_text("dram_bytes_per_launch = 1234\nkernel_source_sha256 = 0\n")
     assert bench.measured_traffic("decode_megakernel", "demo") is None
     assert bench.measured_traffic("decode_megakernel", "absent") is None
+
+
+def test_block_stats_of_the_per_step_time():
+    # three blocks of 64 steps at 0.5, 0.6 and 0.7 ms per step and a partial block of 8 at 0.5:
+    # percentiles over the four blocks' ms per step, linear interpolation
+    marks = [(0, 0.0), (64, 32.0), (128, 32.0 + 38.4), (192, 32.0 + 38.4 + 44.8), (200, 32.0 + 38.4 + 44.8 + 4.0)]
+    d = bench.block_stats(marks)
+    assert d["blocks"] == 4 and d["block_steps"] == bench.BLOCK_STEPS
+    assert abs(d["median"] - 0.55) < 1e-9          # between 0.5 and 0.6 of (0.5, 0.5, 0.6, 0.7)
+    assert abs(d["p10"] - 0.5) < 1e-9
+    assert abs(d["p90"] - 0.67) < 1e-9              # 0.6 + 0.7 * (0.7 - 0.6)
+    # a region of one block has no distribution
+    assert bench.block_stats([(0, 0.0), (40, 20.0)]) is None
