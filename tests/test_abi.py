@@ -1,5 +1,6 @@
 """The C-ABI library on the CPU: it loads, exports every function include/tinfer.h declares, and
-its host-side logic (configuration checks, packed sizes, status strings) behaves as documented.
+its host-side logic (configuration checks, packed sizes, status strings, the prefill product's
+argument checks) behaves as documented.
 No compute call is made here."""
 import ctypes
 import os
@@ -89,3 +90,20 @@ def test_status_strings():
     assert T.status_string(T.TINFER_OK) == "ok"
     assert T.status_string(T.TINFER_ERR_TIMEOUT) == "device wait timed out"
     assert T.status_string(99) == "unknown status"
+
+
+def test_gemm_arguments_are_checked_before_any_device_work():
+    # every case below fails the host checks of tinfer_op_gemm_bf16 before its first CUDA call, so
+    # the stand-in addresses are never dereferenced and the test is safe with or without a GPU
+    a = 1 << 20  # 16-byte aligned stand-in address
+    bad = T.TINFER_ERR_INVALID_ARG
+    assert T.tinfer_op_gemm_bf16(0, 4, 64, a, a, a) == bad        # empty M
+    assert T.tinfer_op_gemm_bf16(4, 0, 64, a, a, a) == bad        # empty N
+    assert T.tinfer_op_gemm_bf16(4, 4, 0, a, a, a) == bad         # empty K
+    assert T.tinfer_op_gemm_bf16(4, 4, 12, a, a, a) == bad        # K not a multiple of 8 (row stride)
+    assert T.tinfer_op_gemm_bf16(4, 4, 64, a + 2, a, a) == bad    # X base not 16-byte aligned
+    assert T.tinfer_op_gemm_bf16(4, 4, 64, a, a + 8, a) == bad    # W base not 16-byte aligned
+    assert T.tinfer_op_gemm_bf16(4, 4, 64, a, a, a + 2) == bad    # Y not 4-byte aligned
+    assert T.tinfer_op_gemm_bf16(4, 4, 64, None, a, a) == bad
+    assert T.tinfer_op_gemm_bf16(4, 4, 64, a, None, a) == bad
+    assert T.tinfer_op_gemm_bf16(4, 4, 64, a, a, None) == bad
